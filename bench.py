@@ -1,0 +1,506 @@
+"""Benchmark of the MSDA sampling core (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decoder_bf16] [--accum fp32|native|auto] [--all]
+
+One step = one pass of the whole hot path over one batch: forward
+(msda_forward), then backward (msda_backward: zero or widen of the grad_value
+accumulator, gather + scatter kernel, and for the fp32 accumulator the
+rounding pass).  Inputs are resident in HBM; the L2 is flushed (a 512 MB
+write) between steps, outside the timed events.  The metric is (b, q, m)
+output vectors per second over the timed steps (higher is better).
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(weak scaling, no data-path collective: the path shards over batches); the
+step time is the max over ranks and the value is the units of all ranks over
+that time.
+
+--impl reference times the fp64 CPU oracle (test infrastructure) on the host
+cores on a bounded sample of the same workload.
+--all prints one extra JSON line per named workload with forward, backward and
+fwd+bwd times (not the contract line).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "MSDA fwd+bwd ms and (b,q,m) outputs/s; achieved HBM GB/s vs GB300 peak"
+UNIT = "(b,q,m) outputs/s"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# byte model (algorithmic bytes per launch)
+
+def inbounds_corners(wl: W.Workload, inp) -> int:
+    """Number of (sample, corner) pairs whose corner lies inside its level, on
+    the binary32 pixel coordinate the kernels use."""
+    loc = W.to_f64(inp["sampling_locations"], wl.dtype)
+    n = 0
+    for l, (h, w) in enumerate(wl.shapes):
+        # exact in fp64 for binary32 inputs and sides <= 8192, then one rounding
+        x = np.floor((loc[:, :, :, l, :, 0] * w - 0.5).astype(np.float32))
+        y = np.floor((loc[:, :, :, l, :, 1] * h - 0.5).astype(np.float32))
+        for dy in (0, 1):
+            for dx in (0, 1):
+                xx, yy = x + dx, y + dy
+                n += int(np.count_nonzero((xx >= 0) & (xx < w) & (yy >= 0) & (yy < h)))
+    return n
+
+
+def byte_model(wl: W.Workload, corners: int) -> dict:
+    es = W.ESIZE[wl.dtype]
+    n_value = wl.B * wl.S * wl.M * wl.D
+    loc = wl.samples * 2 * es
+    attn = wl.samples * es
+    rowio = wl.units * wl.D * es            # out, or grad_out
+    gather = corners * wl.D * es
+    fwd = gather + loc + attn + rowio
+    # backward kernel: corner reads + atomic payload at the value dtype, grad_out, params, param grads
+    bwd_kernel = 2 * gather + rowio + 2 * (loc + attn)
+    bwd = bwd_kernel + n_value * es          # + one full grad_value write
+    return {"forward": fwd, "backward": bwd_kernel, "bwd_total": bwd, "zero": n_value * es,
+            "convert": n_value * (4 + es), "step": fwd + bwd}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scale_deformable_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, accum: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the kernel source as it is now."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[f"{workload}/{accum}/{kernel}"]
+        if e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+class GpuStep:
+    """Preallocated buffers and the raw C-ABI calls of one fwd+bwd step."""
+
+    def __init__(self, wl: W.Workload, inp, accum: str, device):
+        import torch
+
+        import scale_deformable_attention_gb300 as msda
+        from scale_deformable_attention_gb300 import _lib
+
+        self.torch = torch
+        self.msda = msda
+        self.lib = _lib.lib()
+        self.wl = wl
+        self.device = device
+        t = W.to_torch(inp, wl.dtype, device)
+        self.t = t
+        self.out = torch.empty((wl.B, wl.Qn, wl.M * wl.D), dtype=t["value"].dtype, device=device)
+        self.gv = torch.empty_like(t["value"])
+        self.gl = torch.empty_like(t["sampling_locations"])
+        self.ga = torch.empty_like(t["attention_weights"])
+        self.dims = (wl.B, wl.S, wl.M, wl.D, wl.L, wl.K, wl.Qn)
+        self.dt = msda.DTYPE_CODE[t["value"].dtype]
+        self.accum = _lib.ACCUM[accum]
+        need = int(self.lib.msda_backward_workspace_size(self.dt, self.accum, *self.dims))
+        self.ws = torch.empty(max(need // 4, 1), dtype=torch.float32, device=device)
+        self.ws_bytes = need
+        self.resolved = _lib.ACCUM_NAMES[int(self.lib.msda_resolve_accum(self.dt, self.accum, *self.dims))]
+        p = lambda x: x.data_ptr()  # noqa: E731
+        self.fargs = (self.dt, *self.dims, p(t["value"]), p(t["spatial_shapes"]), p(t["level_start_index"]),
+                      p(t["sampling_locations"]), p(t["attention_weights"]), p(self.out))
+        self.bargs = (self.dt, self.accum, 0, *self.dims, p(t["value"]), p(t["spatial_shapes"]),
+                      p(t["level_start_index"]), p(t["sampling_locations"]), p(t["attention_weights"]),
+                      p(t["grad_out"]), p(self.gv), p(self.gl), p(self.ga), p(self.ws), self.ws_bytes)
+        self.flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def stream(self):
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def forward(self):
+        from scale_deformable_attention_gb300 import _lib
+
+        _lib.check(self.lib.msda_forward(*self.fargs, self.stream()))
+
+    def backward(self):
+        from scale_deformable_attention_gb300 import _lib
+
+        _lib.check(self.lib.msda_backward(*self.bargs, self.stream()))
+
+    def step(self):
+        self.forward()
+        self.backward()
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def timed(self, fn, steps: int):
+        """Device time of `fn` per step with the L2 flushed before each one (ms)."""
+        torch = self.torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            self.flush()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+
+def _dist():
+    import torch.distributed as dist
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    return dist if ws > 1 else None, int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def run_ours(args):
+    import torch
+
+    dist, rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import scale_deformable_attention_gb300 as msda
+
+    wl = W.WORKLOADS[args.workload]
+    wl = wl.with_(seed=wl.seed + 1000 * rank) if rank else wl
+    inp = W.make_inputs(wl)
+    accum = args.accum or wl.accum
+    st = GpuStep(wl, inp, accum, device)
+    corners = inbounds_corners(wl, inp)
+    model = byte_model(wl, corners)
+
+    for _ in range(max(args.warmup, 3)):
+        st.flush()
+        st.step()
+    torch.cuda.synchronize()
+    # launches per step, from one traced step
+    msda.trace_enable(64)
+    st.step()
+    recs, _ = msda.trace_read()
+    launches_per_step = len(recs)
+
+    msda.trace_enable(min(4 * args.steps + 8, 16384))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    uuid = str(torch.cuda.get_device_properties(device).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    with ClockSampler(uuid) as clk:
+        times = st.timed(st.step, args.steps)
+    torch.cuda.synchronize()
+    recs, dropped = msda.trace_read()
+    msda.trace_enable(0)
+    total_ms = float(sum(times))
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = wl.units * world * args.steps / (total_ms / 1e3)
+
+    # per-kernel durations over the traced part of the timed region
+    per = {}
+    for name, ms, work in recs:
+        per.setdefault(name, []).append(ms)
+    dom = max(per, key=lambda k: sum(per[k])) if per else None
+    peak, peak_kind = peaks()
+    roof = None
+    if dom:
+        avg_ms = statistics.mean(per[dom])
+        alg = model["convert"] if dom == "convert" else model[dom]
+        achieved = alg / (avg_ms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom, wl.name, st.resolved),
+                "algorithmic_bytes": alg, "avg_launch_ms": round(avg_ms, 5), "peak_source": peak_kind,
+                "launches_traced": len(per[dom])}
+    kernels = {k: {"launches": len(v), "avg_ms": round(statistics.mean(v), 5),
+                   "share": round(sum(v) / sum(sum(x) for x in per.values()), 4)} for k, v in per.items()}
+
+    e2e = run_e2e(st, inp, args) if not args.no_e2e else None
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "Q": wl.Qn, "M": wl.M, "D": wl.D, "L": wl.L, "K": wl.K,
+                       "S": wl.S, "spatial_shapes": [list(s) for s in wl.shapes], "accum": st.resolved,
+                       "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MB write, outside the timed events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
+            "roofline": roof, "kernels": kernels, "bytes_per_step_model": model["step"],
+            "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
+            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped,
+        }
+        print(json.dumps(line), flush=True)
+    if args.all and rank == 0:
+        for name in W.WORKLOADS:
+            print(json.dumps(run_workload_table(name, args, device)), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(st: GpuStep, inp, args):
+    """Same metric through the public API with host inputs: each step copies
+    its inputs host->device from pinned memory, runs forward + backward and
+    reads the results back device->host."""
+    torch = st.torch
+    msda = st.msda
+    wl = st.wl
+    host = {k: v.pin_memory() for k, v in W.to_torch(inp, wl.dtype, "cpu").items()}
+    outs = {"out": torch.empty(tuple(st.out.shape), dtype=st.out.dtype).pin_memory(),
+            "gv": torch.empty(tuple(st.gv.shape), dtype=st.gv.dtype).pin_memory(),
+            "gl": torch.empty(tuple(st.gl.shape), dtype=st.gl.dtype).pin_memory(),
+            "ga": torch.empty(tuple(st.ga.shape), dtype=st.ga.dtype).pin_memory()}
+    bi = sum(t.numel() * t.element_size() for t in host.values())
+    bo = sum(t.numel() * t.element_size() for t in outs.values())
+    dev = {k: torch.empty_like(v, device=st.device) for k, v in host.items()}
+    accum = st.resolved
+    steps = max(10, min(args.e2e_steps, args.steps))
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        out = msda.forward(dev["value"], host["spatial_shapes"], dev["level_start_index"], dev["sampling_locations"],
+                           dev["attention_weights"], validate=False)
+        gv, gl, ga = msda.backward(dev["value"], host["spatial_shapes"], dev["level_start_index"],
+                                   dev["sampling_locations"], dev["attention_weights"], dev["grad_out"], accum=accum,
+                                   validate=False)
+        outs["out"].copy_(out, non_blocking=True)
+        outs["gv"].copy_(gv, non_blocking=True)
+        outs["gl"].copy_(gl, non_blocking=True)
+        outs["ga"].copy_(ga, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(wl.units / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+            "d2h_bytes_per_step": int(bo), "ms_per_step": round(ms, 4), "steps": steps}
+
+
+def cpu_baseline(wl: W.Workload, inp, budget_s: float):
+    """The fp64 oracle on the host cores, on whole fwd+bwd passes of the same
+    inputs repeated for about `budget_s` seconds."""
+    import oracle
+
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.forward(inp, wl.dtype)
+        oracle.backward(inp, wl.dtype)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(wl.units * reps / el, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} full fwd+bwd passes of {wl.name} ({wl.units} units each) in {el:.1f} s"}
+
+
+def run_workload_table(name: str, args, device):
+    """Forward / backward / fwd+bwd device times of one named workload."""
+    import torch
+
+    wl = W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    out = {}
+    accums = ["native", "fp32"] if wl.dtype != "f32" else ["auto"]
+    corners = inbounds_corners(wl, inp)
+    model = byte_model(wl, corners)
+    peak, _ = peaks()
+    for accum in accums:
+        st = GpuStep(wl, inp, accum, device)
+        n = 5 if name == "stress_bf16" else 50
+        for _ in range(3):
+            st.step()
+        tf = statistics.median(st.timed(st.forward, n))
+        tb = statistics.median(st.timed(st.backward, n))
+        ts = statistics.median(st.timed(st.step, n))
+        out[accum] = {"fwd_ms": round(tf, 4), "bwd_ms": round(tb, 4), "step_ms": round(ts, 4),
+                      "fwd_units_per_s": round(wl.units / (tf / 1e3), 1),
+                      "bwd_units_per_s": round(wl.units / (tb / 1e3), 1),
+                      "step_units_per_s": round(wl.units / (ts / 1e3), 1),
+                      "fwd_frac_of_8TBs": round(model["forward"] / (tf / 1e3) / 8e12, 4),
+                      "bwd_frac_of_8TBs": round(model["bwd_total"] / (tb / 1e3) / 8e12, 4),
+                      "fwd_frac_of_measured": round(model["forward"] / (tf / 1e3) / 1e9 / peak, 4),
+                      "bwd_frac_of_measured": round(model["bwd_total"] / (tb / 1e3) / 1e9 / peak, 4)}
+        del st
+        torch.cuda.empty_cache()
+    return {"table": name, "units": wl.units, "corners_inside": corners, "bytes_model": model, "results": out}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    wl = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(wl)
+    # size each step's sample (a prefix of the queries) so the run takes ~budget
+    t0 = time.perf_counter()
+    oracle.forward(inp, wl.dtype)
+    oracle.backward(inp, wl.dtype)
+    t_full = time.perf_counter() - t0
+    per_step = args.ref_budget / max(1, args.steps + args.warmup)
+    q = int(max(1, min(wl.Qn, wl.Qn * per_step / max(t_full, 1e-9))))
+    sub = dict(inp)
+    for k in ("sampling_locations", "attention_weights", "grad_out"):
+        sub[k] = np.ascontiguousarray(inp[k][:, :q])
+    units = wl.B * q * wl.M
+    for _ in range(args.warmup):
+        oracle.forward(sub, wl.dtype)
+        oracle.backward(sub, wl.dtype)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(sub, wl.dtype)
+        oracle.backward(sub, wl.dtype)
+    el = time.perf_counter() - t0
+    value = units * args.steps / el
+    sample = f"first {q} of {wl.Qn} queries of every batch ({units} units) per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "Q": wl.Qn, "M": wl.M, "D": wl.D, "L": wl.L, "K": wl.K},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decoder_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--accum", choices=["auto", "native", "fp32"], default=None,
+                    help="grad_value accumulator (default: the workload's)")
+    ap.add_argument("--all", action="store_true", help="also print per-workload fwd/bwd tables")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

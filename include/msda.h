@@ -1,0 +1,195 @@
+/*
+ * msda.h -- C ABI of the GB300 (sm_103a) multi-scale deformable attention
+ * sampling core.
+ *
+ * The operation (msda-triton README, "The operator"): for every batch b,
+ * query q and head m, the bracketed term of
+ *
+ *     MSDA(q) = sum_m W_m [ sum_l sum_k A_mlqk * x_l(phi_l(p_q) + dp_mlqk) ]
+ *
+ * i.e. out[b,q,m,:] = sum_{l,k} A[b,q,m,l,k] * bilinear_l(value[b,:,m,:], loc[b,q,m,l,k]).
+ * The projections W_m, the offset/weight linears and the softmax are not part
+ * of it.
+ *
+ * Sampling convention (README, "Kernel design", last paragraph; course ch. 4,
+ * "Bilinear sampling"): x_im = x * W_l - 0.5, y_im = y * H_l - 0.5 (the
+ * grid_sample align_corners=False convention); x0 = floor(x_im),
+ * lx = x_im - x0 and likewise for y; the four corners (y0+i, x0+j) get the
+ * weights (i ? ly : 1-ly) * (j ? lx : 1-lx); a corner outside
+ * [0, W_l) x [0, H_l) contributes nothing and receives no gradient (zero
+ * padding).  The cell decision floor(x_im) is taken on x_im computed in
+ * binary32 as the single rounding of x * W_l - 0.5; everything is accumulated
+ * in fp32 and rounded once (round to nearest even) to the I/O dtype.
+ *
+ * Layouts (README, "Quickstart"; course ch. 4, "Setup" and "The main loop").
+ * All tensors are dense, row-major, in device memory owned by the caller:
+ *
+ *   value                    [B, S, M, D]        S = sum_l H_l * W_l
+ *   spatial_shapes           [L, 2] int64        rows (H_l, W_l)
+ *   level_start_index        [L]    int64        first pyramid row of level l
+ *   sampling_locations       [B, Q, M, L, K, 2]  (x, y), normalised to [0, 1]
+ *   attention_weights        [B, Q, M, L, K]
+ *   out                      [B, Q, M * D]
+ *   grad_out                 [B, Q, M * D]
+ *   grad_value               [B, S, M, D]
+ *   grad_sampling_locations  [B, Q, M, L, K, 2]
+ *   grad_attention_weights   [B, Q, M, L, K]
+ *
+ * One dtype (msda_dtype) applies to every floating-point tensor of a call.
+ * Index arithmetic is 64-bit (course ch. 4, "The int64 casts are
+ * load-bearing").
+ *
+ * Calls are asynchronous on `stream`: they validate their arguments on the
+ * host, enqueue kernels and return.  They never synchronise, never allocate
+ * device memory and never read device memory from the host, so they can be
+ * enqueued while a stream is being captured into a CUDA graph (README,
+ * "Caveats": the operator is graph capturable).  A status other than MSDA_OK
+ * means nothing was enqueued, except MSDA_ERR_CUDA, which reports a failed
+ * launch.  Pointers are not retained after the call returns.
+ *
+ * Device-resident spatial shapes cannot be checked on the host without a
+ * synchronisation.  The kernels therefore check every level themselves
+ * (H_l, W_l in [1, 2^24], start >= 0, start + H_l*W_l <= S); a level that
+ * fails is treated as empty (its samples read nothing and receive zero
+ * gradient) and sets a bit that msda_device_errors() reports.
+ */
+#ifndef MSDA_H
+#define MSDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (binary-compatible with cudaStream_t / CUstream); NULL is the
+ * legacy default stream. */
+typedef struct CUstream_st* msda_stream_t;
+
+typedef enum { MSDA_F32 = 0, MSDA_F16 = 1, MSDA_BF16 = 2 } msda_dtype;
+
+/* Accumulator of grad_value for fp16 / bf16 (course ch. 5, "The fix:
+ * accumulate in FP32, downcast at the end"; README, "Kernel design" item 3).
+ * NATIVE: relaxed 16-bit vector atomic adds straight into grad_value.
+ * FP32:   relaxed fp32 vector atomic adds into a caller-provided fp32
+ *         workspace, then one rounding pass into grad_value.
+ * AUTO:   the choice msda_resolve_accum() returns.
+ * For MSDA_F32 all three are the same path (fp32 atomics, no workspace). */
+typedef enum { MSDA_ACCUM_AUTO = 0, MSDA_ACCUM_NATIVE = 1, MSDA_ACCUM_FP32 = 2 } msda_accum;
+
+typedef enum {
+    MSDA_OK = 0,
+    MSDA_ERR_INVALID_ARG = 1,  /* negative or inconsistent sizes, NULL pointer, unknown enum or flag */
+    MSDA_ERR_UNSUPPORTED = 2,  /* L, K, L*K or D above the compiled limits below */
+    MSDA_ERR_MISALIGNED = 3,   /* a pointer not aligned to its element size */
+    MSDA_ERR_WORKSPACE = 4,    /* FP32 accumulation without a large enough 16-byte aligned workspace */
+    MSDA_ERR_CUDA = 5          /* a CUDA runtime call or launch failed; see msda_last_error() */
+} msda_status;
+
+/* Compiled limits. */
+#define MSDA_MAX_LEVELS 16
+#define MSDA_MAX_POINTS 64      /* K */
+#define MSDA_MAX_SAMPLES 256    /* L * K */
+#define MSDA_MAX_CHANNELS 1024  /* D */
+
+/* Flags of msda_backward. */
+#define MSDA_BWD_ACCUMULATE 1u  /* add this call's gradient to grad_value instead of overwriting it */
+
+/*
+ * Forward (course ch. 4, "The forward kernel, line by line"; README,
+ * "Kernel design" item 1).  Writes out[B, Q, M*D].  B == 0, Q == 0, M == 0 or
+ * D == 0 enqueue nothing and return MSDA_OK (course ch. 4, "The wrapper":
+ * empty inputs are handled without launching).
+ *
+ * Requirements: B, S, M, D, Q >= 0; 1 <= L <= MSDA_MAX_LEVELS;
+ * 1 <= K <= MSDA_MAX_POINTS; L*K <= MSDA_MAX_SAMPLES; D <= MSDA_MAX_CHANNELS;
+ * every non-empty tensor pointer non-NULL and aligned to its element size.
+ * Rows of 16-byte multiples with 16-byte aligned value/out take the vector
+ * path; anything else takes the element-wise path, with identical results.
+ */
+msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K,
+                         int64_t Q, const void* value, const int64_t* spatial_shapes,
+                         const int64_t* level_start_index, const void* sampling_locations,
+                         const void* attention_weights, void* out, msda_stream_t stream);
+
+/* Workspace bytes msda_backward needs for (dt, mode) and the value size:
+ * B*S*M*D*4 when the resolved accumulator is FP32 for fp16/bf16, else 0. */
+size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
+                                    int64_t L, int64_t K, int64_t Q);
+
+/* The accumulator AUTO resolves to for this problem (NATIVE or FP32; a
+ * NATIVE or FP32 request is returned unchanged; MSDA_F32 returns NATIVE). */
+msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
+                              int64_t L, int64_t K, int64_t Q);
+
+/*
+ * Backward (course ch. 5, "What the backward pass must produce", "Scatter
+ * needs atomics", "sem=relaxed"; README, "Kernel design" items 2 and 3).
+ *
+ *   grad_attention_weights[p]     = <g, sampled_p>
+ *   grad_sampling_locations[p][0] = A_p * W_l * <g, d sampled_p / d x_im>
+ *   grad_sampling_locations[p][1] = A_p * H_l * <g, d sampled_p / d y_im>
+ *   grad_value[b, corner, m, :]  += A_p * w_corner * g       (inside corners only)
+ *
+ * with g = grad_out[b, q, m*D:(m+1)*D] and the location derivative that of the
+ * zero-padded bilinear interpolant inside the cell chosen by floor.
+ * grad_sampling_locations and grad_attention_weights are overwritten.
+ * grad_value is zeroed on `stream` first, unless `flags` has
+ * MSDA_BWD_ACCUMULATE, in which case the gradient is added to its contents.
+ * grad_value is summed by relaxed atomic adds, so its bits may differ between
+ * runs (course ch. 5, "Atomics make gradients nondeterministic").
+ *
+ * `workspace` (device, 16-byte aligned, >= msda_backward_workspace_size()
+ * bytes) is used only by the FP32 accumulator and may be NULL otherwise; its
+ * contents on entry are irrelevant and are clobbered.
+ * B == 0, Q == 0, M == 0 or D == 0: only the zeroing of grad_value runs.
+ * Requirements as msda_forward.
+ */
+msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M,
+                          int64_t D, int64_t L, int64_t K, int64_t Q, const void* value,
+                          const int64_t* spatial_shapes, const int64_t* level_start_index,
+                          const void* sampling_locations, const void* attention_weights, const void* grad_out,
+                          void* grad_value, void* grad_sampling_locations, void* grad_attention_weights,
+                          void* workspace, size_t workspace_bytes, msda_stream_t stream);
+
+/* Message for the last non-OK status returned on the calling thread ("" if none). */
+const char* msda_last_error(void);
+
+/* Short name of a status code. */
+const char* msda_status_string(msda_status s);
+
+/* Device-side error bits raised by kernels on the current device since the
+ * last clear (bit 0: a level failed its shape check).  Synchronises the
+ * device.  clear != 0 resets the bits. */
+msda_status msda_device_errors(uint32_t* bits, int clear);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int msda_version(void);
+
+/*
+ * Kernel trace.  While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its own stream (no
+ * synchronisation).  msda_trace_read() waits for the recorded events and
+ * returns one record per launch, oldest first, then forgets them.  Launches
+ * beyond `capacity` are counted in `dropped` but not recorded.  Enabling
+ * creates 2*capacity events on the current device; capacity 0 disables and
+ * destroys them.  Not thread-safe against concurrent msda_* calls.
+ */
+typedef struct {
+    int kernel;        /* MSDA_KERNEL_* */
+    float ms;          /* elapsed time between the two events */
+    int64_t work;      /* (b,q,m) units for fwd/bwd, elements for zero/convert */
+} msda_trace_record;
+
+enum { MSDA_KERNEL_FORWARD = 0, MSDA_KERNEL_BACKWARD = 1, MSDA_KERNEL_ZERO = 2, MSDA_KERNEL_CONVERT = 3,
+       MSDA_KERNEL_COUNT = 4 };
+
+msda_status msda_trace_enable(int capacity);
+int msda_trace_read(msda_trace_record* records, int max_records, int* dropped);
+const char* msda_kernel_name(int kernel);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSDA_H */

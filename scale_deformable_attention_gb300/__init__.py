@@ -1,0 +1,214 @@
+"""GB300 (sm_103a) multi-scale deformable attention sampling core.
+
+The bracketed term of MSDA(q) = sum_m W_m [sum_l sum_k A_mlqk x_l(phi_l(p_q) + dp_mlqk)]
+(msda-triton README, "The operator") and its three gradients, computed by the
+hand-written CUDA kernels of ``libmsda.so`` behind the C ABI of
+``include/msda.h``.  This module only marshals torch tensors into that ABI:
+it checks shapes, dtypes and devices, makes inputs contiguous, allocates
+outputs (and the fp32 workspace of the FP32 accumulator) with torch, and
+passes raw pointers and the current CUDA stream.
+
+Entry points:
+
+* ``multi_scale_deformable_attention(value, spatial_shapes, level_start_index,
+  sampling_locations, attention_weights, fp32_grad_accum=None)`` -- the
+  differentiable operator (signature of the README's quickstart);
+* ``forward(...)`` / ``backward(...)`` -- the two C-ABI calls;
+* ``device_errors()``, ``trace_enable()`` / ``trace_read()`` -- diagnostics.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import ACCUM, BWD_ACCUMULATE, MsdaError
+
+__all__ = ["multi_scale_deformable_attention", "forward", "backward", "workspace_size", "resolve_accum",
+           "device_errors", "trace_enable", "trace_read", "MsdaError", "DTYPE_CODE"]
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def level_start_index_of(spatial_shapes: torch.Tensor) -> torch.Tensor:
+    """Exclusive prefix sum of H_l * W_l (what the README's wrapper computes when
+    level_start_index is None)."""
+    hw = spatial_shapes[:, 0] * spatial_shapes[:, 1]
+    return torch.cat([hw.new_zeros(1), hw.cumsum(0)[:-1]])
+
+
+def _prepare(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, validate: bool):
+    if value.dim() != 4:
+        raise ValueError(f"value must be [B, S, M, D], got shape {tuple(value.shape)}")
+    B, S, M, D = value.shape
+    if sampling_locations.dim() != 6 or sampling_locations.shape[-1] != 2:
+        raise ValueError(f"sampling_locations must be [B, Q, M, L, K, 2], got {tuple(sampling_locations.shape)}")
+    Q, L, K = sampling_locations.shape[1], sampling_locations.shape[3], sampling_locations.shape[4]
+    if tuple(sampling_locations.shape) != (B, Q, M, L, K, 2):
+        raise ValueError(f"sampling_locations shape {tuple(sampling_locations.shape)} does not match value "
+                         f"[B={B}, S, M={M}, D]")
+    if tuple(attention_weights.shape) != (B, Q, M, L, K):
+        raise ValueError(f"attention_weights must be {(B, Q, M, L, K)}, got {tuple(attention_weights.shape)}")
+    if value.dtype not in DTYPE_CODE:
+        raise TypeError(f"unsupported dtype {value.dtype}; use float32, float16 or bfloat16")
+    for name, t in (("sampling_locations", sampling_locations), ("attention_weights", attention_weights)):
+        if t.dtype != value.dtype:
+            raise TypeError(f"{name} is {t.dtype} but value is {value.dtype}; all float tensors share one dtype")
+    dev = value.device
+    if dev.type != "cuda":
+        raise ValueError("the operator runs on CUDA tensors only (there is no CPU implementation)")
+    for name, t in (("sampling_locations", sampling_locations), ("attention_weights", attention_weights)):
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, value on {dev}")
+    if spatial_shapes.dim() != 2 or spatial_shapes.shape != (L, 2):
+        raise ValueError(f"spatial_shapes must be [L={L}, 2], got {tuple(spatial_shapes.shape)}")
+    if validate:
+        hw = spatial_shapes.to("cpu", torch.int64)
+        if bool((hw <= 0).any()):
+            raise ValueError(f"spatial_shapes must be positive, got {hw.tolist()}")
+        tot = int((hw[:, 0] * hw[:, 1]).sum())
+        if tot != S:
+            raise ValueError(f"value has S={S} rows but sum(H*W) over spatial_shapes is {tot}")
+    spatial_shapes = spatial_shapes.to(dev, torch.int64).contiguous()
+    if level_start_index is None:
+        level_start_index = level_start_index_of(spatial_shapes)
+    else:
+        if level_start_index.shape != (L,):
+            raise ValueError(f"level_start_index must be [L={L}], got {tuple(level_start_index.shape)}")
+        level_start_index = level_start_index.to(dev, torch.int64).contiguous()
+    dims = (B, S, M, D, L, K, Q)
+    return (value.contiguous(), spatial_shapes, level_start_index, sampling_locations.contiguous(),
+            attention_weights.contiguous(), dims)
+
+
+def forward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_index: Optional[torch.Tensor],
+            sampling_locations: torch.Tensor, attention_weights: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+            validate: bool = True) -> torch.Tensor:
+    """out[B, Q, M*D] on the current stream (C ABI ``msda_forward``)."""
+    value, ss, lsi, loc, attn, dims = _prepare(value, spatial_shapes, level_start_index, sampling_locations,
+                                               attention_weights, validate)
+    B, S, M, D, L, K, Q = dims
+    if out is None:
+        out = torch.empty((B, Q, M * D), dtype=value.dtype, device=value.device)
+    elif out.shape != (B, Q, M * D) or out.dtype != value.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, Q, M*D] tensor of value's dtype")
+    with torch.cuda.device(value.device):
+        _lib.check(_lib.lib().msda_forward(DTYPE_CODE[value.dtype], *dims, _ptr(value), _ptr(ss), _ptr(lsi),
+                                           _ptr(loc), _ptr(attn), _ptr(out), _stream(value.device)))
+    return out
+
+
+def resolve_accum(dtype: torch.dtype, accum: str, dims) -> str:
+    """Which grad_value accumulator ("native" or "fp32") the backward uses."""
+    r = _lib.lib().msda_resolve_accum(DTYPE_CODE[dtype], ACCUM[accum], *dims)
+    return _lib.ACCUM_NAMES[r]
+
+
+def workspace_size(dtype: torch.dtype, accum: str, dims) -> int:
+    return int(_lib.lib().msda_backward_workspace_size(DTYPE_CODE[dtype], ACCUM[accum], *dims))
+
+
+def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_index: Optional[torch.Tensor],
+             sampling_locations: torch.Tensor, attention_weights: torch.Tensor, grad_out: torch.Tensor, *,
+             accum: str = "auto", grad_value: Optional[torch.Tensor] = None, accumulate: bool = False,
+             workspace: Optional[torch.Tensor] = None, validate: bool = True
+             ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(grad_value, grad_sampling_locations, grad_attention_weights) (C ABI ``msda_backward``).
+
+    ``accum``: "auto" | "native" | "fp32" accumulator of grad_value for fp16 / bf16.
+    ``accumulate``: add into the given ``grad_value`` instead of overwriting it.
+    """
+    value, ss, lsi, loc, attn, dims = _prepare(value, spatial_shapes, level_start_index, sampling_locations,
+                                               attention_weights, validate)
+    B, S, M, D, L, K, Q = dims
+    if accum not in ACCUM:
+        raise ValueError(f"accum must be one of {sorted(ACCUM)}, got {accum!r}")
+    if grad_out.shape != (B, Q, M * D) or grad_out.dtype != value.dtype or grad_out.device != value.device:
+        raise ValueError(f"grad_out must be a [B, Q, M*D] {value.dtype} tensor on {value.device}")
+    grad_out = grad_out.contiguous()
+    if grad_value is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs grad_value")
+        grad_value = torch.empty_like(value)
+    elif grad_value.shape != value.shape or grad_value.dtype != value.dtype or not grad_value.is_contiguous():
+        raise ValueError("grad_value must be a contiguous tensor shaped and typed like value")
+    grad_loc = torch.empty_like(loc)
+    grad_attn = torch.empty_like(attn)
+    need = workspace_size(value.dtype, accum, dims)
+    if need and workspace is None:
+        workspace = torch.empty(need // 4, dtype=torch.float32, device=value.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    flags = BWD_ACCUMULATE if accumulate else 0
+    with torch.cuda.device(value.device):
+        _lib.check(_lib.lib().msda_backward(
+            DTYPE_CODE[value.dtype], ACCUM[accum], flags, *dims, _ptr(value), _ptr(ss), _ptr(lsi), _ptr(loc),
+            _ptr(attn), _ptr(grad_out), _ptr(grad_value), _ptr(grad_loc), _ptr(grad_attn), _ptr(workspace),
+            ws_bytes, _stream(value.device)))
+    return grad_value, grad_loc, grad_attn
+
+
+class _MSDAFunction(torch.autograd.Function):
+    """Autograd wrapper (course ch. 5, "The autograd wrapper"): saves the inputs
+    and recomputes the bilinear setup in the backward kernel; the backward is
+    not itself differentiable."""
+
+    @staticmethod
+    def forward(ctx, value, spatial_shapes, level_start_index, sampling_locations, attention_weights, accum):
+        out = forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights)
+        ss = spatial_shapes.to(value.device, torch.int64)
+        lsi = level_start_index_of(ss) if level_start_index is None else level_start_index.to(value.device, torch.int64)
+        ctx.save_for_backward(value, ss, lsi, sampling_locations, attention_weights)
+        ctx.accum = accum
+        return out
+
+    @staticmethod
+    @torch.autograd.function.once_differentiable
+    def backward(ctx, grad_out):
+        value, ss, lsi, loc, attn = ctx.saved_tensors
+        gv, gl, ga = backward(value, ss, lsi, loc, attn, grad_out, accum=ctx.accum, validate=False)
+        return gv, None, None, gl, ga, None
+
+
+def multi_scale_deformable_attention(value: torch.Tensor, spatial_shapes: torch.Tensor,
+                                     level_start_index: Optional[torch.Tensor], sampling_locations: torch.Tensor,
+                                     attention_weights: torch.Tensor, fp32_grad_accum: Optional[bool] = None
+                                     ) -> torch.Tensor:
+    """Differentiable MSDA sampling core, out[B, Q, M*D].
+
+    ``fp32_grad_accum``: None lets the library choose the grad_value
+    accumulator for fp16 / bf16; True forces the fp32 workspace; False forces
+    native 16-bit atomic adds.
+    """
+    accum = "auto" if fp32_grad_accum is None else ("fp32" if fp32_grad_accum else "native")
+    return _MSDAFunction.apply(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, accum)
+
+
+def device_errors(clear: bool = True) -> int:
+    """Error bits raised by kernels on the current device (bit 0: a level failed
+    its shape check; bit 1: a parameter copy timed out).  Synchronises."""
+    v = ctypes.c_uint32(0)
+    _lib.check(_lib.lib().msda_device_errors(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
+
+
+def trace_enable(capacity: int) -> None:
+    """Bracket every kernel launch by CUDA events (capacity launches; 0 disables)."""
+    _lib.check(_lib.lib().msda_trace_enable(int(capacity)))
+
+
+def trace_read(max_records: int = 1 << 16):
+    """[(kernel name, ms, work)] of the traced launches since the last read (waits for them)."""
+    recs = (_lib.TraceRecord * max_records)()
+    dropped = ctypes.c_int(0)
+    n = _lib.lib().msda_trace_read(recs, max_records, ctypes.byref(dropped))
+    return [(_lib.KERNEL_NAMES.get(r.kernel, str(r.kernel)), float(r.ms), int(r.work)) for r in recs[:n]], dropped.value

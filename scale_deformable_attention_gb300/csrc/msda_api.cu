@@ -1,0 +1,559 @@
+// msda_api.cu -- the C ABI declared in include/msda.h: host-side validation,
+// launch planning and kernel launches on the caller's stream.  No call here
+// synchronises, allocates device memory or reads device memory, except
+// msda_device_errors() and msda_trace_read(), which are documented to wait.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "msda_launch.cuh"
+
+using msda::KernelArgs;
+using msda::Plan;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+
+thread_local char g_msg[512];
+
+msda_status fail(msda_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+msda_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MSDA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+size_t esize(msda_dtype dt) { return dt == MSDA_F32 ? 4 : 2; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// ---- per-device state ----
+
+struct DeviceInfo {
+    bool init = false;
+    int sms = 0;
+    unsigned* err = nullptr;  // device address of g_msda_err on this device
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+}  // namespace
+
+// Device error word (see msda_device_errors).  One copy per device; its device
+// address is looked up once per device with cudaGetSymbolAddress.
+__device__ unsigned int g_msda_err;
+
+namespace {
+
+msda_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MSDA_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_msda_err);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+        d.err = static_cast<unsigned*>(p);
+        d.init = true;
+    }
+    *out = &d;
+    return MSDA_OK;
+}
+
+// ---- kernel trace ----
+
+struct Trace {
+    int cap = 0, n = 0, dropped = 0, device = -1;
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> kernel;
+    std::vector<int64_t> work;
+};
+Trace g_trace;
+std::mutex g_trace_mu;
+
+struct TraceScope {
+    int slot = -1;
+    cudaStream_t st;
+    TraceScope(cudaStream_t s) : st(s) {
+        if (g_trace.cap == 0) return;
+        std::lock_guard<std::mutex> lk(g_trace_mu);
+        if (g_trace.n >= g_trace.cap) {
+            ++g_trace.dropped;
+            return;
+        }
+        slot = g_trace.n++;
+        cudaEventRecord(g_trace.ev[2 * slot], st);
+    }
+    void end(int kernel, int64_t work) {
+        if (slot < 0) return;
+        cudaEventRecord(g_trace.ev[2 * slot + 1], st);
+        g_trace.kernel[slot] = kernel;
+        g_trace.work[slot] = work;
+    }
+};
+
+// ---- tuning overrides (sweeps only): MSDA_TUNE="C=4,P=2,params=bulk|ld|direct" ----
+
+struct Tune {
+    int C = 0, P = 0, params = -1;
+};
+const Tune& tune() {
+    static Tune t = [] {
+        Tune r;
+        const char* s = getenv("MSDA_TUNE");
+        if (!s) return r;
+        char buf[256];
+        snprintf(buf, sizeof(buf), "%s", s);
+        for (char* tok = strtok(buf, ","); tok; tok = strtok(nullptr, ",")) {
+            if (!strncmp(tok, "C=", 2)) r.C = atoi(tok + 2);
+            else if (!strncmp(tok, "P=", 2)) r.P = atoi(tok + 2);
+            else if (!strcmp(tok, "params=bulk")) r.params = msda::PARAMS_SMEM_BULK;
+            else if (!strcmp(tok, "params=ld")) r.params = msda::PARAMS_SMEM_LD;
+            else if (!strcmp(tok, "params=direct")) r.params = msda::PARAMS_DIRECT;
+        }
+        return r;
+    }();
+    return t;
+}
+
+int ilog2(int v) {
+    int r = 0;
+    while ((1 << r) < v) ++r;
+    return r;
+}
+
+// ---- validation ----
+
+struct Dims {
+    int64_t B, S, M, D, L, K, Q;
+    int64_t units;    // B*Q*M
+    int64_t n_value;  // B*S*M*D
+    int64_t n_param;  // B*Q*M*L*K
+};
+
+msda_status check_dims(msda_dtype dt, Dims& d) {
+    if (dt != MSDA_F32 && dt != MSDA_F16 && dt != MSDA_BF16) return fail(MSDA_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+    if (d.B < 0 || d.S < 0 || d.M < 0 || d.D < 0 || d.L < 0 || d.K < 0 || d.Q < 0)
+        return fail(MSDA_ERR_INVALID_ARG, "negative size (B=%lld S=%lld M=%lld D=%lld L=%lld K=%lld Q=%lld)",
+                    (long long)d.B, (long long)d.S, (long long)d.M, (long long)d.D, (long long)d.L, (long long)d.K,
+                    (long long)d.Q);
+    if (d.L == 0 || d.K == 0) return fail(MSDA_ERR_INVALID_ARG, "L and K must be at least 1");
+    if (d.L > MSDA_MAX_LEVELS) return fail(MSDA_ERR_UNSUPPORTED, "L=%lld above %d", (long long)d.L, MSDA_MAX_LEVELS);
+    if (d.K > MSDA_MAX_POINTS) return fail(MSDA_ERR_UNSUPPORTED, "K=%lld above %d", (long long)d.K, MSDA_MAX_POINTS);
+    if (d.L * d.K > MSDA_MAX_SAMPLES)
+        return fail(MSDA_ERR_UNSUPPORTED, "L*K=%lld above %d", (long long)(d.L * d.K), MSDA_MAX_SAMPLES);
+    if (d.D > MSDA_MAX_CHANNELS) return fail(MSDA_ERR_UNSUPPORTED, "D=%lld above %d", (long long)d.D, MSDA_MAX_CHANNELS);
+    int64_t t;
+    if (!mul_ok(d.B, d.Q, &t) || !mul_ok(t, d.M, &d.units) || !mul_ok(d.units, d.L * d.K * 2, &t) ||
+        !mul_ok(t, 8, &t) || !mul_ok(d.units, d.D, &t) || !mul_ok(t, 8, &t))
+        return fail(MSDA_ERR_INVALID_ARG, "B*Q*M*L*K overflows 64 bits");
+    d.n_param = d.units * d.L * d.K;
+    if (!mul_ok(d.B, d.S, &t) || !mul_ok(t, d.M, &t) || !mul_ok(t, d.D, &d.n_value) || !mul_ok(d.n_value, 8, &t))
+        return fail(MSDA_ERR_INVALID_ARG, "B*S*M*D overflows 64 bits");
+    return MSDA_OK;
+}
+
+msda_status check_ptr(const void* p, bool needed, size_t align, const char* name) {
+    if (!needed) return MSDA_OK;
+    if (!p) return fail(MSDA_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, align)) return fail(MSDA_ERR_MISALIGNED, "%s is not aligned to %zu bytes", name, align);
+    return MSDA_OK;
+}
+
+// ---- launch planning ----
+
+// Lanes per row C and vectors per lane NV for nvec slots per row: the
+// smallest lane waste with NV <= 4, ties towards C = 4.
+void pick_c(int nvec, int* C, int* NV) {
+    int bestC = 32, bestNV = (nvec + 31) / 32, bestWaste = 1 << 30, bestDist = 1 << 30;
+    for (int c = 1; c <= 32; c <<= 1) {
+        const int nv = (nvec + c - 1) / c;
+        if (nv > 4) continue;
+        const int waste = c * nv - nvec;
+        const int dist = abs(ilog2(c) - 2);
+        if (waste < bestWaste || (waste == bestWaste && dist < bestDist)) {
+            bestC = c, bestNV = nv, bestWaste = waste, bestDist = dist;
+        }
+    }
+    *C = bestC;
+    *NV = bestNV;
+}
+
+msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, const void* loc, const void* attn, Plan& pl,
+                      KernelArgs& a) {
+    const int es = (int)esize(dt);
+    const int epv = vec ? 16 / es : 1;
+    const int nvec = (int)(d.D / epv);
+    int C, NV;
+    pick_c(nvec, &C, &NV);
+    if ((int64_t)C * NV * epv < d.D)
+        return fail(MSDA_ERR_UNSUPPORTED, "D=%lld too large for %s rows (at most %d channels)", (long long)d.D,
+                    vec ? "16-byte" : "unaligned", 32 * 4 * epv);
+    const int LK = (int)(d.L * d.K);
+    const Tune& t = tune();
+    if (t.C > 0 && (t.C & (t.C - 1)) == 0 && t.C <= 32 && (int64_t)t.C * 4 * epv >= d.D) {
+        C = t.C;
+        NV = (nvec + C - 1) / C;
+    }
+    // point lanes: enough lanes to fill the GPU, within one warp (C*P <= 32) and L*K
+    int P = 1;
+    const int64_t target = (int64_t)sms * 1536;
+    while (P * C < 32 && P * 2 <= LK && d.units * C * P < target) P *= 2;
+    if (t.P > 0 && (t.P & (t.P - 1)) == 0 && t.P * C <= 32) P = t.P;
+    const int tp = C * P;
+    const int tpb = msda::kBlockThreads / tp;
+    // parameter staging: one bulk copy when both chunks are 16-byte pieces
+    const int64_t loc_unit = (int64_t)LK * 2 * es, attn_unit = (int64_t)LK * es;
+    const bool v16 = (loc_unit % 16 == 0) && (attn_unit % 16 == 0) && aligned(loc, 16) && aligned(attn, 16);
+    const size_t smem = (size_t)(((tpb * loc_unit) + 15) / 16 * 16 + tpb * attn_unit + 16);
+    int mode = v16 ? msda::PARAMS_SMEM_BULK : msda::PARAMS_SMEM_LD;
+    if (t.params >= 0) mode = t.params;
+    if (mode == msda::PARAMS_SMEM_BULK && !v16) mode = msda::PARAMS_SMEM_LD;
+    if (smem > 48 * 1024) mode = msda::PARAMS_DIRECT;
+
+    a.B = d.B, a.S = d.S, a.M = d.M, a.D = d.D, a.L = d.L, a.K = d.K, a.Q = d.Q;
+    a.n_units = d.units;
+    a.lc = ilog2(C);
+    a.lp = ilog2(P);
+    a.nvec = nvec;
+    a.tpb = tpb;
+    a.param_mode = mode;
+    a.loc_vec16 = v16 ? 1 : 0;
+
+    pl.block = dim3(msda::kBlockThreads);
+    const int64_t blocks = (d.units + tpb - 1) / tpb;
+    if (blocks > 0x7fffffffLL) return fail(MSDA_ERR_UNSUPPORTED, "too many units (%lld)", (long long)d.units);
+    pl.grid = dim3((unsigned)blocks);
+    pl.smem_params = mode != msda::PARAMS_DIRECT;
+    pl.smem = pl.smem_params ? smem : 0;
+    pl.nv = NV;
+    pl.vec = vec;
+    return MSDA_OK;
+}
+
+int grid_for(int64_t n, int sms) {
+    const int64_t want = (n + msda::kBlockThreads - 1) / msda::kBlockThreads;
+    const int64_t cap = (int64_t)sms * 8;
+    return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// zero kernel (non-template; lives here, its only user)
+
+namespace msda {
+__global__ void __launch_bounds__(kBlockThreads) msda_zero_kernel(unsigned char* p, long long nbytes) {
+    // head up to 16-byte alignment, 16-byte body, tail
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(p);
+    const long long head = min((long long)((16 - (addr & 15)) & 15), nbytes);
+    const long long body = (nbytes - head) / 16;
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    if (tid < head) p[tid] = 0;
+    uint4* q = reinterpret_cast<uint4*>(p + head);
+    for (long long i = tid; i < body; i += nth) q[i] = make_uint4(0u, 0u, 0u, 0u);
+    const long long tail0 = head + body * 16;
+    if (tid < nbytes - tail0) p[tail0 + tid] = 0;
+}
+}  // namespace msda
+
+namespace {
+msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
+    if (nbytes <= 0) return MSDA_OK;
+    TraceScope ts(st);
+    msda::msda_zero_kernel<<<grid_for(nbytes / 16 + 1, sms), msda::kBlockThreads, 0, st>>>(
+        static_cast<unsigned char*>(p), nbytes);
+    ts.end(MSDA_KERNEL_ZERO, nbytes);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "zero kernel launch");
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+
+extern "C" {
+
+int msda_version(void) { return kVersion; }
+
+const char* msda_last_error(void) { return g_msg; }
+
+const char* msda_status_string(msda_status s) {
+    switch (s) {
+    case MSDA_OK: return "MSDA_OK";
+    case MSDA_ERR_INVALID_ARG: return "MSDA_ERR_INVALID_ARG";
+    case MSDA_ERR_UNSUPPORTED: return "MSDA_ERR_UNSUPPORTED";
+    case MSDA_ERR_MISALIGNED: return "MSDA_ERR_MISALIGNED";
+    case MSDA_ERR_WORKSPACE: return "MSDA_ERR_WORKSPACE";
+    case MSDA_ERR_CUDA: return "MSDA_ERR_CUDA";
+    }
+    return "MSDA_STATUS_UNKNOWN";
+}
+
+const char* msda_kernel_name(int k) {
+    switch (k) {
+    case MSDA_KERNEL_FORWARD: return "forward";
+    case MSDA_KERNEL_BACKWARD: return "backward";
+    case MSDA_KERNEL_ZERO: return "zero";
+    case MSDA_KERNEL_CONVERT: return "convert";
+    }
+    return "unknown";
+}
+
+msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K, int64_t Q,
+                         const void* value, const int64_t* spatial_shapes, const int64_t* level_start_index,
+                         const void* sampling_locations, const void* attention_weights, void* out,
+                         msda_stream_t stream) {
+    g_msg[0] = 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    msda_status s = check_dims(dt, d);
+    if (s != MSDA_OK) return s;
+    if (d.units == 0 || D == 0) return MSDA_OK;  // empty output: nothing to launch
+    const size_t es = esize(dt);
+    if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
+        (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
+        (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
+        (s = check_ptr(sampling_locations, true, es, "sampling_locations")) ||
+        (s = check_ptr(attention_weights, true, es, "attention_weights")) || (s = check_ptr(out, true, es, "out")))
+        return s;
+    DeviceInfo* di = nullptr;
+    if ((s = device_info(&di))) return s;
+    const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(out, 16);
+    KernelArgs a{};
+    Plan pl{};
+    if ((s = make_plan(dt, d, vec, di->sms, sampling_locations, attention_weights, pl, a))) return s;
+    a.value = value;
+    a.shapes = spatial_shapes;
+    a.starts = level_start_index;
+    a.loc = sampling_locations;
+    a.attn = attention_weights;
+    a.out = out;
+    a.err = di->err;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    TraceScope ts(st);
+    switch (dt) {
+    case MSDA_F32: msda::launch_forward<float>(a, pl, st); break;
+    case MSDA_F16: msda::launch_forward<__half>(a, pl, st); break;
+    default: msda::launch_forward<__nv_bfloat16>(a, pl, st); break;
+    }
+    ts.end(MSDA_KERNEL_FORWARD, d.units);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "forward kernel launch");
+}
+
+msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L,
+                              int64_t K, int64_t Q) {
+    (void)B, (void)M, (void)D;
+    if (dt == MSDA_F32) return MSDA_ACCUM_NATIVE;
+    if (mode == MSDA_ACCUM_NATIVE || mode == MSDA_ACCUM_FP32) return mode;
+    // AUTO: native 16-bit reductions unless many samples land on each pixel,
+    // where per-add rounding of bf16 would dominate the error.
+    const double contrib = S > 0 ? 4.0 * (double)Q * (double)L * (double)K / (double)S : 0.0;
+    if (dt == MSDA_BF16 && contrib > 8.0) return MSDA_ACCUM_FP32;
+    return MSDA_ACCUM_NATIVE;
+}
+
+size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
+                                    int64_t L, int64_t K, int64_t Q) {
+    if (dt != MSDA_F16 && dt != MSDA_BF16) return 0;
+    if (B < 0 || S < 0 || M < 0 || D < 0) return 0;
+    if (msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q) != MSDA_ACCUM_FP32) return 0;
+    int64_t n;
+    if (!mul_ok(B, S, &n) || !mul_ok(n, M, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 4, &n)) return SIZE_MAX;
+    return (size_t)n;
+}
+
+msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M, int64_t D,
+                          int64_t L, int64_t K, int64_t Q, const void* value, const int64_t* spatial_shapes,
+                          const int64_t* level_start_index, const void* sampling_locations,
+                          const void* attention_weights, const void* grad_out, void* grad_value,
+                          void* grad_sampling_locations, void* grad_attention_weights, void* workspace,
+                          size_t workspace_bytes, msda_stream_t stream) {
+    g_msg[0] = 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    msda_status s = check_dims(dt, d);
+    if (s != MSDA_OK) return s;
+    if (mode != MSDA_ACCUM_AUTO && mode != MSDA_ACCUM_NATIVE && mode != MSDA_ACCUM_FP32)
+        return fail(MSDA_ERR_INVALID_ARG, "unknown accumulator mode %d", (int)mode);
+    if (flags & ~MSDA_BWD_ACCUMULATE) return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const bool accumulate = (flags & MSDA_BWD_ACCUMULATE) != 0;
+    const size_t es = esize(dt);
+    const bool work = d.units > 0 && D > 0;
+    if ((s = check_ptr(grad_value, d.n_value > 0, es, "grad_value"))) return s;
+    if (work) {
+        if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
+            (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
+            (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
+            (s = check_ptr(sampling_locations, true, es, "sampling_locations")) ||
+            (s = check_ptr(attention_weights, true, es, "attention_weights")) ||
+            (s = check_ptr(grad_out, true, es, "grad_out")) ||
+            (s = check_ptr(grad_sampling_locations, true, es, "grad_sampling_locations")) ||
+            (s = check_ptr(grad_attention_weights, true, es, "grad_attention_weights")))
+            return s;
+    }
+    const msda_accum acc = msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q);
+    const bool use_ws = dt != MSDA_F32 && acc == MSDA_ACCUM_FP32 && work && d.n_value > 0;
+    if (use_ws) {
+        const size_t need = (size_t)d.n_value * 4;
+        if (!workspace || workspace_bytes < need)
+            return fail(MSDA_ERR_WORKSPACE, "FP32 accumulation needs a %zu-byte workspace (got %zu at %p)", need,
+                        workspace_bytes, workspace);
+        if (!aligned(workspace, 16)) return fail(MSDA_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+    }
+    if (d.n_value == 0 && !work) return MSDA_OK;
+
+    DeviceInfo* di = nullptr;
+    if ((s = device_info(&di))) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    // grad_value (or the workspace) must start from zero / from grad_value
+    if (!use_ws) {
+        if (!accumulate && (s = launch_zero(grad_value, d.n_value * (int64_t)es, di->sms, st))) return s;
+        if (!work) return MSDA_OK;
+    } else if (!accumulate) {
+        if ((s = launch_zero(workspace, d.n_value * 4, di->sms, st))) return s;
+    } else {
+        TraceScope ts(st);
+        const int grid = grid_for(d.n_value, di->sms);
+        if (dt == MSDA_F16)
+            msda::launch_widen<__half>(static_cast<const __half*>(grad_value), static_cast<float*>(workspace),
+                                       d.n_value, grid, st);
+        else
+            msda::launch_widen<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(grad_value),
+                                              static_cast<float*>(workspace), d.n_value, grid, st);
+        ts.end(MSDA_KERNEL_CONVERT, d.n_value);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "widen kernel launch");
+    }
+
+    void* acc_buf = use_ws ? workspace : grad_value;
+    const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16) &&
+                     aligned(acc_buf, 16);
+    KernelArgs a{};
+    Plan pl{};
+    if ((s = make_plan(dt, d, vec, di->sms, sampling_locations, attention_weights, pl, a))) return s;
+    a.value = value;
+    a.shapes = spatial_shapes;
+    a.starts = level_start_index;
+    a.loc = sampling_locations;
+    a.attn = attention_weights;
+    a.grad_out = grad_out;
+    a.grad_acc = acc_buf;
+    a.grad_loc = grad_sampling_locations;
+    a.grad_attn = grad_attention_weights;
+    a.err = di->err;
+    {
+        TraceScope ts(st);
+        switch (dt) {
+        case MSDA_F32: msda::launch_backward<float, float>(a, pl, st); break;
+        case MSDA_F16:
+            if (use_ws) msda::launch_backward<__half, float>(a, pl, st);
+            else msda::launch_backward<__half, __half>(a, pl, st);
+            break;
+        default:
+            if (use_ws) msda::launch_backward<__nv_bfloat16, float>(a, pl, st);
+            else msda::launch_backward<__nv_bfloat16, __nv_bfloat16>(a, pl, st);
+            break;
+        }
+        ts.end(MSDA_KERNEL_BACKWARD, d.units);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
+    }
+    if (use_ws) {
+        TraceScope ts(st);
+        const int cvec = aligned(grad_value, 16) ? 1 : 0;
+        const int grid = grid_for(d.n_value / 8 + 1, di->sms);
+        if (dt == MSDA_F16)
+            msda::launch_convert<__half>(static_cast<const float*>(workspace), static_cast<__half*>(grad_value),
+                                         d.n_value, cvec, grid, st);
+        else
+            msda::launch_convert<__nv_bfloat16>(static_cast<const float*>(workspace),
+                                                static_cast<__nv_bfloat16*>(grad_value), d.n_value, cvec, grid, st);
+        ts.end(MSDA_KERNEL_CONVERT, d.n_value);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
+    }
+    return MSDA_OK;
+}
+
+msda_status msda_device_errors(uint32_t* bits, int clear) {
+    g_msg[0] = 0;
+    if (!bits) return fail(MSDA_ERR_INVALID_ARG, "bits is NULL");
+    DeviceInfo* di = nullptr;
+    msda_status s = device_info(&di);
+    if (s) return s;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_msda_err, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+    *bits = v;
+    if (clear) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_msda_err, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    }
+    return MSDA_OK;
+}
+
+msda_status msda_trace_enable(int capacity) {
+    g_msg[0] = 0;
+    if (capacity < 0) return fail(MSDA_ERR_INVALID_ARG, "negative trace capacity");
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    for (cudaEvent_t ev : g_trace.ev) cudaEventDestroy(ev);
+    g_trace = Trace();
+    if (capacity == 0) return MSDA_OK;
+    g_trace.ev.resize(2 * (size_t)capacity);
+    for (auto& ev : g_trace.ev) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) {
+            for (cudaEvent_t x : g_trace.ev)
+                if (x) cudaEventDestroy(x);
+            g_trace = Trace();
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    g_trace.kernel.assign(capacity, -1);
+    g_trace.work.assign(capacity, 0);
+    g_trace.cap = capacity;
+    return MSDA_OK;
+}
+
+int msda_trace_read(msda_trace_record* records, int max_records, int* dropped) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    const int n = g_trace.n < max_records ? g_trace.n : max_records;
+    for (int i = 0; i < n; ++i) {
+        float ms = -1.f;
+        if (cudaEventSynchronize(g_trace.ev[2 * i + 1]) == cudaSuccess)
+            cudaEventElapsedTime(&ms, g_trace.ev[2 * i], g_trace.ev[2 * i + 1]);
+        records[i].kernel = g_trace.kernel[i];
+        records[i].ms = ms;
+        records[i].work = g_trace.work[i];
+    }
+    if (dropped) *dropped = g_trace.dropped + (g_trace.n - n);
+    g_trace.n = 0;
+    g_trace.dropped = 0;
+    return n;
+}
+
+}  // extern "C"

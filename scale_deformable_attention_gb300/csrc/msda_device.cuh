@@ -1,0 +1,675 @@
+// msda_device.cuh -- sm_103a device code of the multi-scale deformable
+// attention sampling core: forward gather, backward gather + relaxed
+// vector-atomic scatter, and the zero / convert helpers of the backward.
+//
+// Work decomposition.  One *unit* is one (b, q, m) output vector of D
+// channels; units are numbered u = (b*Q + q)*M + m, so consecutive units own
+// contiguous rows of out / grad_out and contiguous runs of the sampling
+// parameters (both [.., M, L, K, ..] with m innermost before (l, k)).  A *team*
+// of C*P lanes (C, P powers of two, C*P <= 32, teams never straddle a warp)
+// owns one unit:
+//   * C channel lanes split a D-row into 16-byte vectors (8 bf16/fp16 or 4
+//     fp32 channels; NV vectors per lane), so each corner row is read with
+//     full-width loads over the channel dimension;
+//   * P point lanes split the L*K sampling points of the unit.
+// A block holds 256 / (C*P) consecutive units.  The forward keeps a private
+// fp32 register accumulator per lane and combines the P point lanes with
+// warp shuffles at the end (no cross-block combine); the backward reduces the
+// per-sample dot products over the C channel lanes with warp shuffles and
+// scatters grad_value with relaxed vector reductions (red.global.add.v4.*),
+// which return nothing and impose no ordering; the end of the kernel is the
+// only synchronisation the sums need.
+//
+// This differs from the msda-triton query-block kernel (course ch. 4,
+// "The design question") in that a block owns consecutive flat (b, q, m)
+// units rather than a query block of one (b, m): the parameters of a block
+// are then one contiguous byte range, staged into shared memory with one
+// bulk copy, and the output tile is one contiguous store.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "../../include/msda.h"
+
+namespace msda {
+
+constexpr int kBlockThreads = 256;
+
+// Sampling-parameter staging.
+enum ParamMode : int { PARAMS_DIRECT = 0, PARAMS_SMEM_LD = 1, PARAMS_SMEM_BULK = 2 };
+
+// Device error bits (msda_device_errors).
+constexpr unsigned kErrBadLevel = 1u;
+constexpr unsigned kErrBulkTimeout = 2u;
+
+struct Level {
+    long long start;
+    int H, W;
+    float fH, fW;
+    int ok;
+};
+
+struct KernelArgs {
+    const void* value;
+    const int64_t* shapes;
+    const int64_t* starts;
+    const void* loc;
+    const void* attn;
+    void* out;             // forward output
+    const void* grad_out;  // backward input
+    void* grad_acc;        // backward: grad_value (native) or the fp32 workspace
+    void* grad_loc;
+    void* grad_attn;
+    unsigned* err;         // device error word
+    long long B, S, M, D, L, K, Q;
+    long long n_units;     // B*Q*M
+    int lc, lp;            // log2(C), log2(P)
+    int nvec;              // vectors per D-row
+    int tpb;               // units (teams) per block
+    int param_mode;        // ParamMode
+    int loc_vec16;         // loc / attn chunks can be copied in 16-byte pieces
+};
+
+// ---------------------------------------------------------------------------
+// element types
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float to_f(float v) { return v; }
+    static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+template <typename T>
+__device__ __forceinline__ float ldg_f(const T* p) {
+    return Elem<T>::to_f(__ldg(p));
+}
+
+// Unpack one 16-byte word into fp32 lanes.
+__device__ __forceinline__ void unpack16(const uint4& w, float (&f)[4], const float*) {
+    f[0] = __uint_as_float(w.x);
+    f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z);
+    f[3] = __uint_as_float(w.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& w, float (&f)[8], const __nv_bfloat16*) {
+    // bf16 -> fp32 is exact: the bf16 bits are the upper half of the binary32
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void unpack16(const uint4& w, float (&f)[8], const __half*) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = *reinterpret_cast<const __half2*>(&u[i]);
+        float2 t = __half22float2(h);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, const __nv_bfloat16*) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, const __half*) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// EPV channels of one vector slot, T storage <-> fp32 registers: one 16-byte
+// word (EPV = 16 / sizeof(T)) or one element (EPV = 1).  Loads in flight are
+// kept as raw words (Raw) and widened to fp32 only when consumed.
+template <typename T, int EPV>
+struct Slot {
+    static_assert(EPV == 1 || EPV * sizeof(T) == 16, "a slot is one element or one 16-byte word");
+    using Raw = typename std::conditional<EPV == 1, T, uint4>::type;
+    static __device__ __forceinline__ Raw zero() {
+        if constexpr (EPV == 1) return Elem<T>::from_f(0.f);
+        else return make_uint4(0u, 0u, 0u, 0u);
+    }
+    static __device__ __forceinline__ Raw load_raw(const T* p) {
+        if constexpr (EPV == 1) return __ldg(p);
+        else return __ldg(reinterpret_cast<const uint4*>(p));
+    }
+    static __device__ __forceinline__ void unpack(const Raw& r, float (&f)[EPV]) {
+        if constexpr (EPV == 1) {
+            f[0] = Elem<T>::to_f(r);
+        } else {
+            const T* tag = nullptr;
+            unpack16(r, f, tag);
+        }
+    }
+    static __device__ __forceinline__ void load(const T* p, float (&f)[EPV]) { unpack(load_raw(p), f); }
+    static __device__ __forceinline__ void store(T* p, const float (&f)[EPV]) {
+        if constexpr (EPV == 1) {
+            *p = Elem<T>::from_f(f[0]);
+        } else if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<uint4*>(p) = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+        } else {
+            const T* tag = nullptr;
+            *reinterpret_cast<uint4*>(p) = make_uint4(pack2(f[0], f[1], tag), pack2(f[2], f[3], tag),
+                                                      pack2(f[4], f[5], tag), pack2(f[6], f[7], tag));
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// relaxed reductions (fire-and-forget, no ordering; course ch. 5, "sem=relaxed")
+
+__device__ __forceinline__ void red_v4_f32(float* p, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void red_v4_bf16x2(__nv_bfloat16* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("red.relaxed.gpu.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void red_v4_f16x2(__half* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("red.relaxed.gpu.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void red_f32(float* p, float v) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_bf16(__nv_bfloat16* p, float v) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    unsigned short s = *reinterpret_cast<unsigned short*>(&h);
+    asm volatile("red.relaxed.gpu.global.add.noftz.bf16 [%0], %1;" ::"l"(p), "h"(s) : "memory");
+}
+__device__ __forceinline__ void red_f16(__half* p, float v) {
+    __half h = __float2half_rn(v);
+    unsigned short s = *reinterpret_cast<unsigned short*>(&h);
+    asm volatile("red.relaxed.gpu.global.add.noftz.f16 [%0], %1;" ::"l"(p), "h"(s) : "memory");
+}
+
+// Add EPV fp32 contributions c[] to EPV consecutive ACC elements at p.
+template <typename ACC, int EPV> struct Scatter;
+template <> struct Scatter<float, 4> {
+    static __device__ __forceinline__ void add(float* p, const float (&c)[4]) { red_v4_f32(p, c[0], c[1], c[2], c[3]); }
+};
+template <> struct Scatter<float, 8> {  // fp16/bf16 slot into the fp32 workspace
+    static __device__ __forceinline__ void add(float* p, const float (&c)[8]) {
+        red_v4_f32(p, c[0], c[1], c[2], c[3]);
+        red_v4_f32(p + 4, c[4], c[5], c[6], c[7]);
+    }
+};
+template <> struct Scatter<__nv_bfloat16, 8> {
+    static __device__ __forceinline__ void add(__nv_bfloat16* p, const float (&c)[8]) {
+        const __nv_bfloat16* t = nullptr;
+        red_v4_bf16x2(p, pack2(c[0], c[1], t), pack2(c[2], c[3], t), pack2(c[4], c[5], t), pack2(c[6], c[7], t));
+    }
+};
+template <> struct Scatter<__half, 8> {
+    static __device__ __forceinline__ void add(__half* p, const float (&c)[8]) {
+        const __half* t = nullptr;
+        red_v4_f16x2(p, pack2(c[0], c[1], t), pack2(c[2], c[3], t), pack2(c[4], c[5], t), pack2(c[6], c[7], t));
+    }
+};
+template <> struct Scatter<float, 1> {
+    static __device__ __forceinline__ void add(float* p, const float (&c)[1]) { red_f32(p, c[0]); }
+};
+template <> struct Scatter<__nv_bfloat16, 1> {
+    static __device__ __forceinline__ void add(__nv_bfloat16* p, const float (&c)[1]) { red_bf16(p, c[0]); }
+};
+template <> struct Scatter<__half, 1> {
+    static __device__ __forceinline__ void add(__half* p, const float (&c)[1]) { red_f16(p, c[0]); }
+};
+
+// ---------------------------------------------------------------------------
+// block prologue: level table and parameter staging
+
+// Largest level side for which the binary32 pixel coordinate and the float
+// bound checks below are exact.
+constexpr long long kMaxSide = 1ll << 24;
+
+__device__ __forceinline__ void load_levels(const KernelArgs& a, Level* lv) {
+    const int l = threadIdx.x;
+    if (l < a.L) {
+        const long long H = a.shapes[2 * l], W = a.shapes[2 * l + 1], st = a.starts[l];
+        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
+                        H * W <= a.S - st;
+        Level v;
+        v.start = ok ? st : 0;
+        v.H = ok ? (int)H : 0;
+        v.W = ok ? (int)W : 0;
+        v.fH = (float)v.H;
+        v.fW = (float)v.W;
+        v.ok = ok;
+        lv[l] = v;
+        if (!ok) atomicOr(a.err, kErrBadLevel);
+    }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Stage the sampling parameters of this block's units into shared memory:
+// loc chunk [nu*LK*2] then (16-byte aligned) attn chunk [nu*LK], raw dtype.
+// Returns false only if a bulk copy did not complete within its wait limit.
+template <typename T>
+__device__ __forceinline__ bool stage_params(const KernelArgs& a, unsigned char* sm, long long u0, uint64_t* bar) {
+    const long long LK = a.L * a.K;
+    const long long nu = min((long long)a.tpb, a.n_units - u0);
+    const long long loc_bytes = nu * LK * 2 * (long long)sizeof(T);
+    const long long attn_bytes = nu * LK * (long long)sizeof(T);
+    const long long attn_off = (((long long)a.tpb * LK * 2 * (long long)sizeof(T)) + 15) & ~15ll;
+    const unsigned char* gloc = (const unsigned char*)a.loc + u0 * LK * 2 * (long long)sizeof(T);
+    const unsigned char* gattn = (const unsigned char*)a.attn + u0 * LK * (long long)sizeof(T);
+    if (a.param_mode == PARAMS_SMEM_BULK) {
+        // one-dimensional bulk copies (the 16-byte alignment of both global
+        // ranges and both sizes is checked on the host)
+        const uint32_t b = smem_u32(bar);
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b));
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b),
+                         "r"((uint32_t)(loc_bytes + attn_bytes))
+                         : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(sm)),
+                "l"(gloc), "r"((uint32_t)loc_bytes), "r"(b)
+                : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(sm + attn_off)),
+                "l"(gattn), "r"((uint32_t)attn_bytes), "r"(b)
+                : "memory");
+        }
+        // bounded wait on phase 0 of the barrier; the verdict is made
+        // block-uniform so that every thread takes the same exit
+        uint32_t done = 0;
+        for (int it = 0; it < (1 << 22) && !done; ++it) {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(done)
+                : "r"(b)
+                : "memory");
+        }
+        if (__syncthreads_and((int)done)) return true;
+        // give a copy still in flight a second bounded wait before the block exits
+        for (int it = 0; it < (1 << 22) && !done; ++it) {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(done)
+                : "r"(b)
+                : "memory");
+        }
+        return false;
+    }
+    if (a.param_mode == PARAMS_SMEM_LD) {
+        if (a.loc_vec16) {
+            const uint4* s1 = reinterpret_cast<const uint4*>(gloc);
+            uint4* d1 = reinterpret_cast<uint4*>(sm);
+            for (long long i = threadIdx.x; i < loc_bytes / 16; i += blockDim.x) d1[i] = __ldg(s1 + i);
+            const uint4* s2 = reinterpret_cast<const uint4*>(gattn);
+            uint4* d2 = reinterpret_cast<uint4*>(sm + attn_off);
+            for (long long i = threadIdx.x; i < attn_bytes / 16; i += blockDim.x) d2[i] = __ldg(s2 + i);
+        } else {
+            const T* s1 = reinterpret_cast<const T*>(gloc);
+            T* d1 = reinterpret_cast<T*>(sm);
+            for (long long i = threadIdx.x; i < nu * LK * 2; i += blockDim.x) d1[i] = __ldg(s1 + i);
+            const T* s2 = reinterpret_cast<const T*>(gattn);
+            T* d2 = reinterpret_cast<T*>(sm + attn_off);
+            for (long long i = threadIdx.x; i < nu * LK; i += blockDim.x) d2[i] = __ldg(s2 + i);
+        }
+    }
+    return true;
+}
+
+// Bilinear setup of one sampling point (course ch. 4, "Bilinear sampling";
+// README, "Kernel design": x_im = x * W_l - 0.5, zero padding).
+struct Corners {
+    long long off[4];  // element offsets of the corner rows (y0,x0), (y0,x0+1), (y0+1,x0), (y0+1,x0+1)
+    float w[4];        // bilinear weights of the four corners
+    bool ok[4];        // corner inside the level
+    float lx, ly;
+};
+
+__device__ __forceinline__ void bilinear_setup(const Level& L, float x, float y, long long row_stride, Corners& cr) {
+    // binary32 pixel coordinate, one rounding of x * W - 0.5
+    const float xi = __fmaf_rn(x, L.fW, -0.5f);
+    const float yi = __fmaf_rn(y, L.fH, -0.5f);
+    const float x0f = floorf(xi), y0f = floorf(yi);
+    const float lx = xi - x0f, ly = yi - y0f;
+    // comparisons are false for NaN: a non-finite location has no corner inside
+    const bool vx0 = L.ok && x0f >= 0.f && x0f < L.fW;
+    const bool vx1 = L.ok && x0f >= -1.f && x0f < L.fW - 1.f;
+    const bool vy0 = y0f >= 0.f && y0f < L.fH;
+    const bool vy1 = y0f >= -1.f && y0f < L.fH - 1.f;
+    const int x0 = (vx0 || vx1) ? (int)x0f : 0;
+    const int y0 = (vy0 || vy1) ? (int)y0f : 0;
+    const long long r0 = L.start + (long long)y0 * L.W + x0;
+    cr.off[0] = r0 * row_stride;
+    cr.off[1] = (r0 + 1) * row_stride;
+    cr.off[2] = (r0 + L.W) * row_stride;
+    cr.off[3] = (r0 + L.W + 1) * row_stride;
+    cr.ok[0] = vy0 && vx0;
+    cr.ok[1] = vy0 && vx1;
+    cr.ok[2] = vy1 && vx0;
+    cr.ok[3] = vy1 && vx1;
+    const float hx = 1.f - lx, hy = 1.f - ly;
+    cr.w[0] = hx * hy;
+    cr.w[1] = lx * hy;
+    cr.w[2] = hx * ly;
+    cr.w[3] = lx * ly;
+    cr.lx = lx;
+    cr.ly = ly;
+}
+
+template <typename T, bool SMEM>
+__device__ __forceinline__ void read_params(const KernelArgs& a, const unsigned char* sm, int team, long long u,
+                                            int s, float& x, float& y, float& w) {
+    const long long LK = a.L * a.K;
+    if constexpr (SMEM) {
+        const long long attn_off = (((long long)a.tpb * LK * 2 * (long long)sizeof(T)) + 15) & ~15ll;
+        const T* pl = reinterpret_cast<const T*>(sm) + ((long long)team * LK + s) * 2;
+        const T* pa = reinterpret_cast<const T*>(sm + attn_off) + (long long)team * LK + s;
+        x = Elem<T>::to_f(pl[0]);
+        y = Elem<T>::to_f(pl[1]);
+        w = Elem<T>::to_f(pa[0]);
+    } else {
+        const T* pl = reinterpret_cast<const T*>(a.loc) + (u * LK + s) * 2;
+        const T* pa = reinterpret_cast<const T*>(a.attn) + u * LK + s;
+        x = ldg_f(pl);
+        y = ldg_f(pl + 1);
+        w = ldg_f(pa);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// forward (course ch. 4; README "Kernel design" item 1)
+
+template <typename T, int NV, int EPV, bool SMEM, int U>
+__global__ void __launch_bounds__(kBlockThreads) msda_fwd_kernel(const KernelArgs a) {
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ __align__(8) uint64_t bar;
+    extern __shared__ __align__(16) unsigned char sm[];
+
+    const int lcp = a.lc + a.lp;
+    const int C = 1 << a.lc, P = 1 << a.lp, TP = 1 << lcp;
+    const int team = threadIdx.x >> lcp;
+    const int lt = threadIdx.x & (TP - 1);
+    const int c = lt & (C - 1);
+    const int p = lt >> a.lc;
+    const int LK = (int)(a.L * a.K);
+    const long long u0 = (long long)blockIdx.x * a.tpb;
+    const long long u = u0 + team;
+    const bool active = u < a.n_units;
+
+    load_levels(a, lv);
+    if constexpr (SMEM) {
+        if (!stage_params<T>(a, sm, u0, &bar)) {
+            if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
+            return;  // nothing was written; the host reports the error bit
+        }
+    }
+    __syncthreads();
+
+    const long long b = active ? u / (a.Q * a.M) : 0;
+    const long long m = active ? u % a.M : 0;
+    const long long row_stride = a.M * a.D;
+    const T* vbase = reinterpret_cast<const T*>(a.value) + (b * a.S * a.M + m) * a.D;
+
+    float acc[NV][EPV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[n][e] = 0.f;
+
+    using S_ = Slot<T, EPV>;
+    for (int s0 = 0; s0 < LK; s0 += P * U) {
+        typename S_::Raw vals[U][4][NV];
+        float coef[U][4];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int s = s0 + p + i * P;
+            Corners cr;
+            float x = -4.f, y = -4.f, w = 0.f;
+            int l = 0;
+            if (active && s < LK) {
+                read_params<T, SMEM>(a, sm, team, u, s, x, y, w);
+                l = s / (int)a.K;
+            } else {
+                l = 0;
+            }
+            Level lev = lv[l];
+            if (!(active && s < LK)) lev.ok = 0;
+            bilinear_setup(lev, x, y, row_stride, cr);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                coef[i][k] = cr.ok[k] ? w * cr.w[k] : 0.f;
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    const int j = n * C + c;
+                    vals[i][k][n] = (cr.ok[k] && j < a.nvec) ? S_::load_raw(vbase + cr.off[k] + (long long)j * EPV)
+                                                             : S_::zero();
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    float v[EPV];
+                    S_::unpack(vals[i][k][n], v);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) acc[n][e] = fmaf(coef[i][k], v[e], acc[n][e]);
+                }
+    }
+
+    // combine the P point lanes of the team
+    for (int o = C; o < TP; o <<= 1) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[n][e] += __shfl_xor_sync(0xffffffffu, acc[n][e], o);
+    }
+    if (active && p == 0) {
+        T* o = reinterpret_cast<T*>(a.out) + u * a.D;
+#pragma unroll
+        for (int n = 0; n < NV; ++n) {
+            const int j = n * C + c;
+            if (j < a.nvec) Slot<T, EPV>::store(o + (long long)j * EPV, acc[n]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// backward (course ch. 5; README "Kernel design" items 2, 3)
+
+template <typename T, typename ACC, int NV, int EPV, bool SMEM, int U>
+__global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArgs a) {
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ __align__(8) uint64_t bar;
+    extern __shared__ __align__(16) unsigned char sm[];
+
+    const int lcp = a.lc + a.lp;
+    const int C = 1 << a.lc, P = 1 << a.lp, TP = 1 << lcp;
+    const int team = threadIdx.x >> lcp;
+    const int lt = threadIdx.x & (TP - 1);
+    const int c = lt & (C - 1);
+    const int p = lt >> a.lc;
+    const int LK = (int)(a.L * a.K);
+    const long long u0 = (long long)blockIdx.x * a.tpb;
+    const long long u = u0 + team;
+    const bool active = u < a.n_units;
+
+    load_levels(a, lv);
+    if constexpr (SMEM) {
+        if (!stage_params<T>(a, sm, u0, &bar)) {
+            if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
+            return;
+        }
+    }
+    __syncthreads();
+
+    const long long b = active ? u / (a.Q * a.M) : 0;
+    const long long m = active ? u % a.M : 0;
+    const long long row_stride = a.M * a.D;
+    const long long vofs = (b * a.S * a.M + m) * a.D;
+    const T* vbase = reinterpret_cast<const T*>(a.value) + vofs;
+    ACC* gbase = reinterpret_cast<ACC*>(a.grad_acc) + vofs;
+
+    // this lane's slots of g = grad_out[b, q, m, :]
+    float g[NV][EPV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+        const int j = n * C + c;
+        if (active && j < a.nvec) {
+            Slot<T, EPV>::load(reinterpret_cast<const T*>(a.grad_out) + u * a.D + (long long)j * EPV, g[n]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) g[n][e] = 0.f;
+        }
+    }
+
+    T* gl = reinterpret_cast<T*>(a.grad_loc);
+    T* ga = reinterpret_cast<T*>(a.grad_attn);
+
+    using S_ = Slot<T, EPV>;
+    for (int s0 = 0; s0 < LK; s0 += P * U) {
+        typename S_::Raw vals[U][4][NV];
+        Corners cr[U];
+        float wa[U];
+        bool live[U];
+        float fW[U], fH[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int s = s0 + p + i * P;
+            float x = -4.f, y = -4.f, w = 0.f;
+            int l = 0;
+            live[i] = active && s < LK;
+            if (live[i]) {
+                read_params<T, SMEM>(a, sm, team, u, s, x, y, w);
+                l = s / (int)a.K;
+            }
+            Level lev = lv[l];
+            if (!live[i]) lev.ok = 0;
+            bilinear_setup(lev, x, y, row_stride, cr[i]);
+            wa[i] = w;
+            fW[i] = lev.fW;
+            fH[i] = lev.fH;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    const int j = n * C + c;
+                    vals[i][k][n] = (cr[i].ok[k] && j < a.nvec)
+                                        ? S_::load_raw(vbase + cr[i].off[k] + (long long)j * EPV)
+                                        : S_::zero();
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            // per-lane partial <g, v_corner> over this lane's channels
+            float d[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float t = 0.f;
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    float v[EPV];
+                    S_::unpack(vals[i][k][n], v);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) t = fmaf(g[n][e], v[e], t);
+                }
+                d[k] = t;
+            }
+            const bool any = cr[i].ok[0] || cr[i].ok[1] || cr[i].ok[2] || cr[i].ok[3];
+            const float lx = cr[i].lx, ly = cr[i].ly;
+            // <g, sampled>, <g, d sampled / d x_im>, <g, d sampled / d y_im>
+            float r_a = any ? (cr[i].w[0] * d[0] + cr[i].w[1] * d[1] + cr[i].w[2] * d[2] + cr[i].w[3] * d[3]) : 0.f;
+            float r_x = any ? ((1.f - ly) * (d[1] - d[0]) + ly * (d[3] - d[2])) : 0.f;
+            float r_y = any ? ((1.f - lx) * (d[2] - d[0]) + lx * (d[3] - d[1])) : 0.f;
+            for (int o = 1; o < C; o <<= 1) {
+                r_a += __shfl_xor_sync(0xffffffffu, r_a, o);
+                r_x += __shfl_xor_sync(0xffffffffu, r_x, o);
+                r_y += __shfl_xor_sync(0xffffffffu, r_y, o);
+            }
+            const int s = s0 + p + i * P;
+            if (live[i] && c == 0) {
+                const long long ps = u * LK + s;
+                ga[ps] = Elem<T>::from_f(r_a);
+                gl[2 * ps] = Elem<T>::from_f(wa[i] * fW[i] * r_x);
+                gl[2 * ps + 1] = Elem<T>::from_f(wa[i] * fH[i] * r_y);
+            }
+            // grad_value scatter: A * w_corner * g into the inside corners
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (!cr[i].ok[k]) continue;
+                const float cf = wa[i] * cr[i].w[k];
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    const int j = n * C + c;
+                    if (j < a.nvec) {
+                        float t[EPV];
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) t[e] = cf * g[n][e];
+                        Scatter<ACC, EPV>::add(gbase + cr[i].off[k] + (long long)j * EPV, t);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// zero / convert helpers of the backward
+
+// grad_value[i] = round(ws[i]) for i < n (8 elements per step when aligned)
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(const float* ws, T* gv, long long n, int vec) {
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    long long done = 0;
+    if (vec) {
+        const long long n8 = n / 8;
+        const float4* s = reinterpret_cast<const float4*>(ws);
+        for (long long i = tid; i < n8; i += nth) {
+            const float4 a = __ldcs(s + 2 * i);
+            const float4 b = __ldcs(s + 2 * i + 1);
+            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            Slot<T, 8>::store(gv + 8 * i, f);
+        }
+        done = n8 * 8;
+    }
+    for (long long i = done + tid; i < n; i += nth) gv[i] = Elem<T>::from_f(ws[i]);
+}
+
+// ws[i] = grad_value[i] (accumulating backward with the fp32 workspace)
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_widen_kernel(const T* gv, float* ws, long long n) {
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    for (long long i = tid; i < n; i += nth) ws[i] = Elem<T>::to_f(gv[i]);
+}
+
+}  // namespace msda

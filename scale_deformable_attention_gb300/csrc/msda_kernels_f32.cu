@@ -1,0 +1,8 @@
+// Kernel instantiations for f32 I/O (see msda_device.cuh).
+#define MSDA_INSTANTIATE
+#include "msda_launch.cuh"
+
+namespace msda {
+template void launch_forward<float>(const KernelArgs&, const Plan&, cudaStream_t);
+template void launch_backward<float, float>(const KernelArgs&, const Plan&, cudaStream_t);
+}  // namespace msda

@@ -1,0 +1,92 @@
+// msda_launch.cuh -- host-side launch of the kernel templates: maps a runtime
+// launch plan (vector width, vectors per lane, parameter staging) onto the
+// compiled instantiations.  Each dtype's instantiations live in their own
+// translation unit (msda_kernels_<dtype>.cu) so they compile in parallel.
+#pragma once
+
+#include "msda_device.cuh"
+
+namespace msda {
+
+// Samples per lane whose corner loads are issued together.
+constexpr int kSamplesInFlight = 2;
+
+struct Plan {
+    dim3 grid, block;
+    size_t smem;   // dynamic shared memory (staged parameters)
+    int nv;        // vectors per lane, 1..4
+    bool vec;      // 16-byte slots (else one element per slot)
+    bool smem_params;
+};
+
+#define MSDA_DISPATCH_NV(NVV, ...)                                   \
+    switch (NVV) {                                                   \
+    case 1: { constexpr int NV = 1; __VA_ARGS__; } break;            \
+    case 2: { constexpr int NV = 2; __VA_ARGS__; } break;            \
+    case 3: { constexpr int NV = 3; __VA_ARGS__; } break;            \
+    default: { constexpr int NV = 4; __VA_ARGS__; } break;           \
+    }
+
+template <typename T, int NV, int EPV, bool SM>
+static void fwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    msda_fwd_kernel<T, NV, EPV, SM, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
+}
+
+template <typename T, typename ACC, int NV, int EPV, bool SM>
+static void bwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    msda_bwd_kernel<T, ACC, NV, EPV, SM, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
+}
+
+template <typename T>
+void launch_forward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    constexpr int VE = 16 / sizeof(T);
+    if (pl.vec) {
+        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, true>(a, pl, st))) }
+        else { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, false>(a, pl, st))) }
+    } else {
+        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, 1, true>(a, pl, st))) }
+        else { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, 1, false>(a, pl, st))) }
+    }
+}
+
+template <typename T, typename ACC>
+void launch_backward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    constexpr int VE = 16 / sizeof(T);
+    if (pl.vec) {
+        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, true>(a, pl, st))) }
+        else { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, false>(a, pl, st))) }
+    } else {
+        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, 1, true>(a, pl, st))) }
+        else { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, 1, false>(a, pl, st))) }
+    }
+}
+
+template <typename T>
+void launch_convert(const float* ws, T* gv, long long n, int vec, int grid, cudaStream_t st) {
+    msda_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, vec);
+}
+
+template <typename T>
+void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st) {
+    msda_widen_kernel<T><<<grid, kBlockThreads, 0, st>>>(gv, ws, n);
+}
+
+#ifndef MSDA_INSTANTIATE
+// defined in msda_kernels_<dtype>.cu
+#define MSDA_EXTERN_IO(T)                                                                  \
+    extern template void launch_forward<T>(const KernelArgs&, const Plan&, cudaStream_t); \
+    extern template void launch_backward<T, float>(const KernelArgs&, const Plan&, cudaStream_t);
+MSDA_EXTERN_IO(float)
+MSDA_EXTERN_IO(__half)
+MSDA_EXTERN_IO(__nv_bfloat16)
+#undef MSDA_EXTERN_IO
+#define MSDA_EXTERN_HALF(T)                                                                              \
+    extern template void launch_backward<T, T>(const KernelArgs&, const Plan&, cudaStream_t);           \
+    extern template void launch_convert<T>(const float*, T*, long long, int, int, cudaStream_t);        \
+    extern template void launch_widen<T>(const T*, float*, long long, int, cudaStream_t);
+MSDA_EXTERN_HALF(__half)
+MSDA_EXTERN_HALF(__nv_bfloat16)
+#undef MSDA_EXTERN_HALF
+#endif
+
+}  // namespace msda

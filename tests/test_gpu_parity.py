@@ -1,0 +1,312 @@
+"""CUDA path vs the fp64 oracle on identical seeded inputs, through the C ABI.
+
+Element-by-element parity on every named workload (full size where the oracle
+finishes in seconds; the stress workload on sampled outputs plus size-free
+properties), plus edge cases: ragged query tails, element-wise (non 16-byte)
+rows, misaligned pointers, empty inputs, all-outside samples, pixel centres,
+maximum L*K, large D, device-side shape checks, accumulation and autograd.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from msda_testutil import assert_forward, assert_grad, f64, rel_l2, to_torch
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import scale_deformable_attention_gb300 as msda
+
+    msda._lib.lib()  # raises when the library is not built: no fallback exists
+    msda.device_errors(clear=True)
+    yield
+    assert msda.device_errors(clear=True) == 0, "a kernel raised a device error bit"
+
+
+def _msda():
+    import scale_deformable_attention_gb300 as msda
+
+    return msda
+
+
+@functools.lru_cache(maxsize=None)
+def _case(name: str, **over):
+    wl = W.WORKLOADS[name].with_(**over) if over else W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    return wl, inp
+
+
+@functools.lru_cache(maxsize=None)
+def _oracle(name: str, items=()):
+    wl, inp = _case(name, **dict(items))
+    out = oracle.forward(inp, wl.dtype)
+    gv, gl, ga = oracle.backward(inp, wl.dtype)
+    return out, gv, gl, ga
+
+
+def _run(wl, inp, accum="auto"):
+    msda = _msda()
+    t = to_torch(inp, wl.dtype, DEV)
+    out = msda.forward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                       t["attention_weights"])
+    gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                               t["attention_weights"], t["grad_out"], accum=accum)
+    torch.cuda.synchronize()
+    return out, gv, gl, ga
+
+
+def _check(name, items, accum):
+    wl, inp = _case(name, **dict(items))
+    out, gv, gl, ga = _run(wl, inp, accum)
+    rout, rgv, rgl, rga = _oracle(name, items)
+    assert_forward(wl.dtype, f64(out), rout, f"{name} out")
+    assert_grad(wl.dtype, f64(ga), rga, f"{name} grad_attn")
+    assert_grad(wl.dtype, f64(gl), rgl, f"{name} grad_loc")
+    assert_grad(wl.dtype, f64(gv), rgv, f"{name} grad_value")
+
+
+# name, overrides (as a tuple of pairs, hashable), accumulator
+CASES = [
+    ("tiny_fp32", (), "auto"),
+    ("tiny_fp32", (("dtype", "bf16"),), "native"),
+    ("tiny_fp32", (("dtype", "bf16"),), "fp32"),
+    ("tiny_fp32", (("dtype", "f16"),), "native"),
+    ("tiny_fp32", (("B", 3), ("Q", 257)), "auto"),                      # several blocks + ragged tail
+    ("decoder_bf16", (), "fp32"),
+    ("decoder_bf16", (), "native"),
+    ("decoder_bf16", (("Q", 301), ("B", 3)), "fp32"),                   # ragged tail
+    ("decoder_bf16", (("dtype", "f32"), ("B", 2)), "auto"),
+    ("decoder_bf16", (("dtype", "f16"), ("B", 2)), "native"),
+    ("encoder_fp16", (), "native"),
+    ("encoder_fp16", (), "fp32"),
+    ("oddD_fp32", (), "auto"),
+    ("oddD_fp32", (("dtype", "bf16"), ("B", 2)), "fp32"),
+    ("stress_bf16", (("B", 1), ("Q", 3000), ("shapes", ((96, 128), (48, 64), (24, 32), (12, 16)))), "fp32"),
+]
+
+
+@pytest.mark.parametrize("name,items,accum", CASES, ids=[f"{n}-{dict(i)}-{a}" for n, i, a in CASES])
+def test_parity(name, items, accum):
+    _check(name, items, accum)
+
+
+@pytest.mark.parametrize("dtype,D", [("f32", 5), ("bf16", 6), ("f16", 3), ("f32", 48), ("bf16", 256),
+                                     ("bf16", 1024), ("f32", 512), ("f16", 100)])
+def test_channel_widths(dtype, D):
+    """Element-wise rows (D*esize not a multiple of 16) and wide rows."""
+    wl = W.WORKLOADS["tiny_fp32"].with_(dtype=dtype, D=D, B=2, Q=19, M=3)
+    inp = W.make_inputs(wl)
+    out, gv, gl, ga = _run(wl, inp, "auto")
+    assert_forward(dtype, f64(out), oracle.forward(inp, dtype), f"D={D}")
+    rgv, rgl, rga = oracle.backward(inp, dtype)
+    assert_grad(dtype, f64(gv), rgv, f"D={D} grad_value")
+    assert_grad(dtype, f64(gl), rgl, f"D={D} grad_loc")
+    assert_grad(dtype, f64(ga), rga, f"D={D} grad_attn")
+
+
+@pytest.mark.parametrize("L,K", [(1, 1), (16, 16), (3, 5), (4, 64)])
+def test_levels_points(L, K):
+    shapes = tuple((3 + l, 4 + 2 * l) for l in range(L))
+    wl = W.WORKLOADS["tiny_fp32"].with_(shapes=shapes, K=K, B=2, Q=7, M=2, D=8)
+    inp = W.make_inputs(wl)
+    out, gv, gl, ga = _run(wl, inp)
+    assert_forward("f32", f64(out), oracle.forward(inp, "f32"))
+    rgv, rgl, rga = oracle.backward(inp, "f32")
+    assert_grad("f32", f64(gv), rgv, "grad_value")
+    assert_grad("f32", f64(gl), rgl, "grad_loc")
+    assert_grad("f32", f64(ga), rga, "grad_attn")
+
+
+def test_misaligned_pointers_take_elementwise_path():
+    """value / grad_out starting 2 bytes past a 16-byte boundary: same results."""
+    msda = _msda()
+    wl = W.WORKLOADS["decoder_bf16"].with_(B=1, Q=50)
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, "bf16", DEV)
+    buf = torch.empty(t["value"].numel() + 1, dtype=torch.bfloat16, device=DEV)
+    v = buf[1:].view(t["value"].shape)
+    v.copy_(t["value"])
+    assert v.data_ptr() % 16 != 0
+    out = msda.forward(v, t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                       t["attention_weights"])
+    gbuf = torch.empty(t["grad_out"].numel() + 1, dtype=torch.bfloat16, device=DEV)
+    g = gbuf[1:].view(t["grad_out"].shape)
+    g.copy_(t["grad_out"])
+    gv, gl, ga = msda.backward(v, t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                               t["attention_weights"], g, accum="native")
+    torch.cuda.synchronize()
+    assert_forward("bf16", f64(out), oracle.forward(inp, "bf16"))
+    rgv, rgl, rga = oracle.backward(inp, "bf16")
+    assert_grad("bf16", f64(gv), rgv, "grad_value")
+    assert_grad("bf16", f64(gl), rgl, "grad_loc")
+
+
+def test_empty_inputs():
+    msda = _msda()
+    for over in (dict(B=0), dict(Q=0)):
+        wl = W.WORKLOADS["tiny_fp32"].with_(**over)
+        inp = W.make_inputs(wl)
+        t = to_torch(inp, "f32", DEV)
+        out = msda.forward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                           t["attention_weights"])
+        assert out.numel() == 0
+        gv = torch.full_like(t["value"], 7.0)
+        gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                                   t["attention_weights"], t["grad_out"], grad_value=gv)
+        torch.cuda.synchronize()
+        assert gl.numel() == 0 and ga.numel() == 0
+        assert bool((gv == 0).all()), "the gradient of an empty sum is zero"
+
+
+def test_all_outside_and_pixel_centres():
+    msda = _msda()
+    wl = W.WORKLOADS["tiny_fp32"].with_(B=1, Q=6, M=2, D=8)
+    inp = W.make_inputs(wl)
+    loc = inp["sampling_locations"].copy()
+    loc[:, :3] = np.array([-3.0, 0.5], dtype=np.float32)       # far outside: x_im < -1
+    loc[:, 3, :, 0, :, 0] = (2 + 0.5) / 8                         # pixel centres of level 0
+    loc[:, 3, :, 0, :, 1] = (1 + 0.5) / 6
+    loc[:, 4] = np.float32(np.nan)                                 # non-finite: no corner inside
+    inp = dict(inp, sampling_locations=loc)
+    out, gv, gl, ga = _run(wl, inp)
+    out = f64(out).reshape(1, 6, 2, 8)
+    assert np.all(out[:, :3] == 0) and np.all(out[:, 4] == 0)
+    assert np.all(f64(gl)[:, :3] == 0) and np.all(f64(ga)[:, :3] == 0)
+    assert np.all(f64(gl)[:, 4] == 0) and np.all(f64(ga)[:, 4] == 0)
+    ref = oracle.forward(inp, "f32").reshape(1, 6, 2, 8)
+    assert_forward("f32", out, ref)
+    rgv, rgl, rga = oracle.backward(inp, "f32")
+    assert_grad("f32", f64(gv), rgv, "grad_value")
+    assert_grad("f32", f64(gl), rgl, "grad_loc")
+
+
+def test_bad_device_shapes_are_contained():
+    """A level whose start + H*W exceeds S (skipping the host check) reads
+    nothing, gets zero gradient and raises device error bit 0."""
+    msda = _msda()
+    wl = W.WORKLOADS["tiny_fp32"]
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, "f32", DEV)
+    bad_starts = torch.tensor([0, 50], dtype=torch.int64, device=DEV)   # level 1 (3x4) would end at 62 > 60
+    out = msda.forward(t["value"], t["spatial_shapes"], bad_starts, t["sampling_locations"], t["attention_weights"],
+                       validate=False)
+    torch.cuda.synchronize()
+    assert msda.device_errors(clear=True) & 1
+    # equals the oracle with level 1 removed from every sample (its attention weights zeroed)
+    attn = inp["attention_weights"].copy()
+    attn[:, :, :, 1] = 0
+    ref = oracle.forward(dict(inp, attention_weights=attn), "f32")
+    assert_forward("f32", f64(out), ref)
+
+
+def test_forward_is_deterministic():
+    msda = _msda()
+    wl, inp = _case("decoder_bf16")
+    t = to_torch(inp, "bf16", DEV)
+    args = (t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"], t["attention_weights"])
+    a = msda.forward(*args)
+    b = msda.forward(*args)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype,accum", [("f32", "auto"), ("bf16", "fp32"), ("f16", "native")])
+def test_accumulate_doubles(dtype, accum):
+    """Backward into the previous call's grad_value adds the same gradient again
+    (up to summation order)."""
+    msda = _msda()
+    wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, B=1, Q=120)
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, dtype, DEV)
+    args = (t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"], t["attention_weights"],
+            t["grad_out"])
+    gv1, _, _ = msda.backward(*args, accum=accum)
+    once = gv1.clone()
+    gv2, _, _ = msda.backward(*args, accum=accum, grad_value=gv1, accumulate=True)
+    torch.cuda.synchronize()
+    lim = 1e-6 if dtype == "f32" else 1e-2
+    assert rel_l2(f64(gv2), 2 * f64(once)) <= lim
+
+
+def test_autograd_matches_direct_calls():
+    msda = _msda()
+    wl = W.WORKLOADS["tiny_fp32"].with_(B=2, Q=33)
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, "f32", DEV)
+    v = t["value"].clone().requires_grad_(True)
+    loc = t["sampling_locations"].clone().requires_grad_(True)
+    attn = t["attention_weights"].clone().requires_grad_(True)
+    out = msda.multi_scale_deformable_attention(v, t["spatial_shapes"], None, loc, attn)
+    out.backward(t["grad_out"])
+    gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], None, t["sampling_locations"],
+                               t["attention_weights"], t["grad_out"])
+    assert rel_l2(f64(v.grad), f64(gv)) <= 1e-6
+    assert torch.equal(loc.grad, gl) and torch.equal(attn.grad, ga)
+
+
+def test_noncontiguous_inputs():
+    msda = _msda()
+    wl = W.WORKLOADS["tiny_fp32"].with_(B=2, Q=21)
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, "f32", DEV)
+    # same values, permuted storage
+    loc_nc = t["sampling_locations"].permute(1, 0, 2, 3, 4, 5).contiguous().permute(1, 0, 2, 3, 4, 5)
+    assert not loc_nc.is_contiguous()
+    out = msda.forward(t["value"], t["spatial_shapes"], None, loc_nc, t["attention_weights"])
+    assert_forward("f32", f64(out), oracle.forward(inp, "f32"))
+
+
+def test_adjoint_identity_on_gpu_outputs():
+    """<g, out> = <grad_value, value> = <grad_attn, A> holds at any size."""
+    wl, inp = _case("encoder_fp16")
+    out, gv, gl, ga = _run(wl, inp, "fp32")
+    g = W.to_f64(inp["grad_out"], "f16")
+    lhs = float(np.sum(g * f64(out)))
+    r1 = float(np.sum(f64(gv) * W.to_f64(inp["value"], "f16")))
+    r2 = float(np.sum(f64(ga) * W.to_f64(inp["attention_weights"], "f16")))
+    scale = float(np.sqrt(np.sum(g ** 2) * np.sum(f64(out) ** 2)))
+    assert abs(lhs - r1) <= 1e-2 * scale and abs(lhs - r2) <= 1e-2 * scale
+
+
+@pytest.mark.slow
+def test_stress_full_size_sampled():
+    """The stress workload at full size (B*S*M*D*2 bytes > 2^32): sampled
+    outputs against the oracle, computed one by one."""
+    msda = _msda()
+    wl = W.WORKLOADS["stress_bf16"]
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, "bf16", DEV)
+    out = msda.forward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                       t["attention_weights"])
+    gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                               t["attention_weights"], t["grad_out"], accum="fp32")
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(123)
+    n_units = wl.units
+    units = np.unique(np.concatenate([rng.choice(n_units, 3000, replace=False), [0, n_units - 1]]))
+    ref = oracle.forward_units(inp, "bf16", units)
+    got = f64(out.view(n_units, wl.D)[torch.from_numpy(units).to(DEV)])
+    assert_forward("bf16", got, ref, "stress out (sampled)")
+    rgl, rga = oracle.backward_units(inp, "bf16", units)
+    LK = wl.L * wl.K
+    idx = torch.from_numpy(units).to(DEV)
+    assert_grad("bf16", f64(gl.view(n_units, LK * 2)[idx]), rgl, "stress grad_loc (sampled)")
+    assert_grad("bf16", f64(ga.view(n_units, LK)[idx]), rga, "stress grad_attn (sampled)")
+    # grad_value rows: the last batch (highest byte offsets) and a spread of the rest
+    n_rows = wl.B * wl.S * wl.M
+    rows = np.unique(np.concatenate([rng.choice(n_rows, 1500, replace=False),
+                                     rng.integers(n_rows - wl.S * wl.M, n_rows, 500)]))
+    rgv = oracle.grad_value_rows(inp, "bf16", rows)
+    got = f64(gv.view(n_rows, wl.D)[torch.from_numpy(rows).to(DEV)])
+    assert_grad("bf16", got, rgv, "stress grad_value (sampled rows)")

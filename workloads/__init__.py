@@ -217,3 +217,19 @@ def make_inputs(wl: Workload, *, with_grad: bool = True) -> Dict[str, np.ndarray
 def scaled(name: str, **kw) -> Workload:
     """A named workload with some sizes overridden (for oracle-sized parity cases)."""
     return WORKLOADS[name].with_(**kw)
+
+
+FLOAT_KEYS = ("value", "sampling_locations", "attention_weights", "grad_out")
+
+
+def to_torch(inp: Dict[str, np.ndarray], dtype: str, device):
+    """Same bytes as torch tensors on ``device`` (bf16 raw bits viewed as torch.bfloat16)."""
+    import torch
+
+    out = {}
+    for k, a in inp.items():
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype == "bf16" and k in FLOAT_KEYS:
+            t = t.view(torch.bfloat16)
+        out[k] = t.to(device)
+    return out
