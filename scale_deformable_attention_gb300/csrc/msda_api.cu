@@ -135,6 +135,14 @@ const Tune& tune() {
     return t;
 }
 
+// Multiplier and shift of msda::fdiv for divisor d >= 1 (numerators < 2^31).
+msda::FastDiv fast_div(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return msda::FastDiv{(uint32_t)m, l};
+}
+
 int ilog2(int v) {
     int r = 0;
     while ((1 << r) < v) ++r;
@@ -198,8 +206,8 @@ void pick_c(int nvec, int* C, int* NV) {
     *NV = bestNV;
 }
 
-msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, const void* loc, const void* attn, Plan& pl,
-                      KernelArgs& a) {
+msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool backward, const void* loc,
+                      const void* attn, Plan& pl, KernelArgs& a) {
     const int es = (int)esize(dt);
     const int epv = vec ? 16 / es : 1;
     const int nvec = (int)(d.D / epv);
@@ -214,37 +222,52 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, const voi
         C = t.C;
         NV = (nvec + C - 1) / C;
     }
-    // point lanes: enough lanes to fill the GPU, within one warp (C*P <= 32) and L*K
+    // point lanes: enough lanes to fill the GPU, within one warp (C*P <= 32)
+    // and L*K.  Measured on GB300: the forward wants ~768 lanes per SM (one
+    // resident wave at its register count), the backward at least two point
+    // lanes per unit and ~384 lanes per SM.
     int P = 1;
-    const int64_t target = (int64_t)sms * 1536;
+    const int64_t target = (int64_t)sms * (backward ? 384 : 768);
     while (P * C < 32 && P * 2 <= LK && d.units * C * P < target) P *= 2;
+    if (backward && P == 1 && C < 32 && LK >= 2) P = 2;
     if (t.P > 0 && (t.P & (t.P - 1)) == 0 && t.P * C <= 32) P = t.P;
     const int tp = C * P;
     const int tpb = msda::kBlockThreads / tp;
     // parameter staging: one bulk copy when both chunks are 16-byte pieces
     const int64_t loc_unit = (int64_t)LK * 2 * es, attn_unit = (int64_t)LK * es;
     const bool v16 = (loc_unit % 16 == 0) && (attn_unit % 16 == 0) && aligned(loc, 16) && aligned(attn, 16);
+    if (d.units >= (1ll << 31) || (d.Q * d.M) >= (1ll << 31))
+        return fail(MSDA_ERR_UNSUPPORTED, "B*Q*M=%lld (b,q,m) units: at most 2^31-1 per call", (long long)d.units);
     const size_t smem = (size_t)(((tpb * loc_unit) + 15) / 16 * 16 + tpb * attn_unit + 16);
     int mode = v16 ? msda::PARAMS_SMEM_BULK : msda::PARAMS_SMEM_LD;
     if (t.params >= 0) mode = t.params;
     if (mode == msda::PARAMS_SMEM_BULK && !v16) mode = msda::PARAMS_SMEM_LD;
     if (smem > 48 * 1024) mode = msda::PARAMS_DIRECT;
 
-    a.B = d.B, a.S = d.S, a.M = d.M, a.D = d.D, a.L = d.L, a.K = d.K, a.Q = d.Q;
-    a.n_units = d.units;
+    a.S = d.S;
+    a.slice = d.S * d.M * d.D;
+    a.M = (int)d.M;
+    a.D = (int)d.D;
+    a.L = (int)d.L;
+    a.K = (int)d.K;
+    a.LK = LK;
+    a.n_units = (int)d.units;
+    a.div_qm = fast_div((uint32_t)(d.Q * d.M));
+    a.div_m = fast_div((uint32_t)d.M);
+    a.div_k = fast_div((uint32_t)d.K);
     a.lc = ilog2(C);
     a.lp = ilog2(P);
     a.nvec = nvec;
     a.tpb = tpb;
     a.param_mode = mode;
-    a.loc_vec16 = v16 ? 1 : 0;
 
     pl.block = dim3(msda::kBlockThreads);
     const int64_t blocks = (d.units + tpb - 1) / tpb;
     if (blocks > 0x7fffffffLL) return fail(MSDA_ERR_UNSUPPORTED, "too many units (%lld)", (long long)d.units);
     pl.grid = dim3((unsigned)blocks);
-    pl.smem_params = mode != msda::PARAMS_DIRECT;
-    pl.smem = pl.smem_params ? smem : 0;
+    pl.smem = mode != msda::PARAMS_DIRECT ? smem : 0;
+    // 32-bit element offsets inside one batch slice, with a row of margin
+    pl.wide = a.slice > (1ll << 30);
     pl.nv = NV;
     pl.vec = vec;
     return MSDA_OK;
@@ -341,7 +364,7 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
     const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(out, 16);
     KernelArgs a{};
     Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, sampling_locations, attention_weights, pl, a))) return s;
+    if ((s = make_plan(dt, d, vec, di->sms, false, sampling_locations, attention_weights, pl, a))) return s;
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;
@@ -451,7 +474,7 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
                      aligned(acc_buf, 16);
     KernelArgs a{};
     Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, sampling_locations, attention_weights, pl, a))) return s;
+    if ((s = make_plan(dt, d, vec, di->sms, true, sampling_locations, attention_weights, pl, a))) return s;
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;

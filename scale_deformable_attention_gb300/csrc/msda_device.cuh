@@ -47,11 +47,23 @@ enum ParamMode : int { PARAMS_DIRECT = 0, PARAMS_SMEM_LD = 1, PARAMS_SMEM_BULK =
 constexpr unsigned kErrBadLevel = 1u;
 constexpr unsigned kErrBulkTimeout = 2u;
 
+// n / d for 0 <= n < 2^31 by a multiply-high and a shift (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994:
+// the round-up multiplier m = floor(2^32 (2^l - d) / d) + 1, l = ceil(log2 d),
+// with the 33rd multiplier bit applied as the "+ n").
+struct FastDiv {
+    uint32_t mul, shift;
+};
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) { return (__umulhi(n, f.mul) + n) >> f.shift; }
+
+// One pyramid level in shared memory; offsets are in elements inside the
+// [S, M, D] slice of one batch image.
 struct Level {
-    long long start;
-    int H, W;
+    long long start_md;  // level_start_index * M * D
+    long long w_md;      // W * M * D (one image row)
     float fH, fW;
-    int ok;
+    int ok;              // passed the shape check
+    int pad_;
 };
 
 struct KernelArgs {
@@ -66,13 +78,15 @@ struct KernelArgs {
     void* grad_loc;
     void* grad_attn;
     unsigned* err;         // device error word
-    long long B, S, M, D, L, K, Q;
-    long long n_units;     // B*Q*M
+    long long S;           // pyramid rows
+    long long slice;       // S * M * D: elements of one batch image
+    int M, D, L, K, LK;
+    int n_units;           // B * Q * M (< 2^31)
+    FastDiv div_qm, div_m, div_k;
     int lc, lp;            // log2(C), log2(P)
     int nvec;              // vectors per D-row
     int tpb;               // units (teams) per block
     int param_mode;        // ParamMode
-    int loc_vec16;         // loc / attn chunks can be copied in 16-byte pieces
 };
 
 // ---------------------------------------------------------------------------
@@ -243,48 +257,47 @@ template <> struct Scatter<__half, 1> {
 // bound checks below are exact.
 constexpr long long kMaxSide = 1ll << 24;
 
-__device__ __forceinline__ void load_levels(const KernelArgs& a, Level* lv) {
-    const int l = threadIdx.x;
-    if (l < a.L) {
-        const long long H = a.shapes[2 * l], W = a.shapes[2 * l + 1], st = a.starts[l];
-        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
-                        H * W <= a.S - st;
-        Level v;
-        v.start = ok ? st : 0;
-        v.H = ok ? (int)H : 0;
-        v.W = ok ? (int)W : 0;
-        v.fH = (float)v.H;
-        v.fW = (float)v.W;
-        v.ok = ok;
-        lv[l] = v;
-        if (!ok) atomicOr(a.err, kErrBadLevel);
-    }
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// Stage the sampling parameters of this block's units into shared memory:
-// loc chunk [nu*LK*2] then (16-byte aligned) attn chunk [nu*LK], raw dtype.
-// Returns false only if a bulk copy did not complete within its wait limit.
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done;
+}
+
+// Byte offset of the attention-weight chunk in the staged parameters.
 template <typename T>
-__device__ __forceinline__ bool stage_params(const KernelArgs& a, unsigned char* sm, long long u0, uint64_t* bar) {
-    const long long LK = a.L * a.K;
-    const long long nu = min((long long)a.tpb, a.n_units - u0);
-    const long long loc_bytes = nu * LK * 2 * (long long)sizeof(T);
-    const long long attn_bytes = nu * LK * (long long)sizeof(T);
-    const long long attn_off = (((long long)a.tpb * LK * 2 * (long long)sizeof(T)) + 15) & ~15ll;
-    const unsigned char* gloc = (const unsigned char*)a.loc + u0 * LK * 2 * (long long)sizeof(T);
-    const unsigned char* gattn = (const unsigned char*)a.attn + u0 * LK * (long long)sizeof(T);
+__device__ __forceinline__ int attn_chunk_offset(const KernelArgs& a) {
+    return (a.tpb * a.LK * 2 * (int)sizeof(T) + 15) & ~15;
+}
+
+// Loads the level table into shared memory and stages the block's sampling
+// parameters (loc chunk [nu*LK*2] then the attn chunk, raw dtype) into `sm`:
+// thread 0 issues one-dimensional bulk copies completing on an mbarrier
+// before the level loads, so the two overlap, and waits for them with a
+// bounded number of polls.  Returns the block-uniform verdict (false only if
+// the copy did not complete within the limit).
+template <typename T>
+__device__ __forceinline__ bool prologue(const KernelArgs& a, Level* lv, unsigned char* sm, uint64_t* bar,
+                                         int* verdict, uint32_t u0) {
+    const int tid = threadIdx.x;
+    const int nu = min(a.tpb, a.n_units - (int)u0);
+    const int loc_bytes = nu * a.LK * 2 * (int)sizeof(T);
+    const int attn_bytes = nu * a.LK * (int)sizeof(T);
+    const int attn_off = attn_chunk_offset<T>(a);
+    const unsigned char* gloc = (const unsigned char*)a.loc + (long long)u0 * a.LK * 2 * (long long)sizeof(T);
+    const unsigned char* gattn = (const unsigned char*)a.attn + (long long)u0 * a.LK * (long long)sizeof(T);
+    const uint32_t b = smem_u32(bar);
     if (a.param_mode == PARAMS_SMEM_BULK) {
-        // one-dimensional bulk copies (the 16-byte alignment of both global
-        // ranges and both sizes is checked on the host)
-        const uint32_t b = smem_u32(bar);
-        if (threadIdx.x == 0) {
+        // both global ranges and both sizes are multiples of 16 bytes (host check)
+        if (tid == 0) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b));
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
             asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b),
                          "r"((uint32_t)(loc_bytes + attn_bytes))
                          : "memory");
@@ -299,59 +312,54 @@ __device__ __forceinline__ bool stage_params(const KernelArgs& a, unsigned char*
                 "l"(gattn), "r"((uint32_t)attn_bytes), "r"(b)
                 : "memory");
         }
-        // bounded wait on phase 0 of the barrier; the verdict is made
-        // block-uniform so that every thread takes the same exit
+    } else if (a.param_mode == PARAMS_SMEM_LD) {
+        const T* s1 = reinterpret_cast<const T*>(gloc);
+        T* d1 = reinterpret_cast<T*>(sm);
+        for (int i = tid; i < nu * a.LK * 2; i += blockDim.x) d1[i] = __ldg(s1 + i);
+        const T* s2 = reinterpret_cast<const T*>(gattn);
+        T* d2 = reinterpret_cast<T*>(sm + attn_off);
+        for (int i = tid; i < nu * a.LK; i += blockDim.x) d2[i] = __ldg(s2 + i);
+    }
+    if (tid < a.L) {
+        const long long H = a.shapes[2 * tid], W = a.shapes[2 * tid + 1], st = a.starts[tid];
+        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
+                        H * W <= a.S - st;
+        const long long MD = (long long)a.M * a.D;
+        Level v;
+        v.start_md = ok ? st * MD : 0;
+        v.w_md = ok ? W * MD : 0;
+        v.fH = ok ? (float)H : 0.f;
+        v.fW = ok ? (float)W : 0.f;
+        v.ok = ok;
+        v.pad_ = 0;
+        lv[tid] = v;
+        if (!ok) atomicOr(a.err, kErrBadLevel);
+    }
+    if (a.param_mode == PARAMS_SMEM_BULK && tid == 0) {
         uint32_t done = 0;
-        for (int it = 0; it < (1 << 22) && !done; ++it) {
-            asm volatile(
-                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
-                "selp.u32 %0, 1, 0, p;\n\t}"
-                : "=r"(done)
-                : "r"(b)
-                : "memory");
-        }
-        if (__syncthreads_and((int)done)) return true;
-        // give a copy still in flight a second bounded wait before the block exits
-        for (int it = 0; it < (1 << 22) && !done; ++it) {
-            asm volatile(
-                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
-                "selp.u32 %0, 1, 0, p;\n\t}"
-                : "=r"(done)
-                : "r"(b)
-                : "memory");
-        }
-        return false;
+        for (int it = 0; it < (1 << 22) && !done; ++it) done = mbar_try_wait(b, 0);
+        *verdict = (int)done;
+        // a copy still in flight gets a second bounded wait before the block exits
+        for (int it = 0; it < (1 << 22) && !done; ++it) done = mbar_try_wait(b, 0);
     }
-    if (a.param_mode == PARAMS_SMEM_LD) {
-        if (a.loc_vec16) {
-            const uint4* s1 = reinterpret_cast<const uint4*>(gloc);
-            uint4* d1 = reinterpret_cast<uint4*>(sm);
-            for (long long i = threadIdx.x; i < loc_bytes / 16; i += blockDim.x) d1[i] = __ldg(s1 + i);
-            const uint4* s2 = reinterpret_cast<const uint4*>(gattn);
-            uint4* d2 = reinterpret_cast<uint4*>(sm + attn_off);
-            for (long long i = threadIdx.x; i < attn_bytes / 16; i += blockDim.x) d2[i] = __ldg(s2 + i);
-        } else {
-            const T* s1 = reinterpret_cast<const T*>(gloc);
-            T* d1 = reinterpret_cast<T*>(sm);
-            for (long long i = threadIdx.x; i < nu * LK * 2; i += blockDim.x) d1[i] = __ldg(s1 + i);
-            const T* s2 = reinterpret_cast<const T*>(gattn);
-            T* d2 = reinterpret_cast<T*>(sm + attn_off);
-            for (long long i = threadIdx.x; i < nu * LK; i += blockDim.x) d2[i] = __ldg(s2 + i);
-        }
-    }
-    return true;
+    __syncthreads();
+    return a.param_mode != PARAMS_SMEM_BULK || *verdict != 0;
 }
 
 // Bilinear setup of one sampling point (course ch. 4, "Bilinear sampling";
-// README, "Kernel design": x_im = x * W_l - 0.5, zero padding).
+// README, "Kernel design": x_im = x * W_l - 0.5, zero padding).  Off is the
+// offset type inside one [S, M, D] slice: int when the slice has < 2^31
+// elements, else long long.
+template <typename Off>
 struct Corners {
-    long long off[4];  // element offsets of the corner rows (y0,x0), (y0,x0+1), (y0+1,x0), (y0+1,x0+1)
-    float w[4];        // bilinear weights of the four corners
-    bool ok[4];        // corner inside the level
+    Off off[4];   // element offsets of (y0,x0), (y0,x0+1), (y0+1,x0), (y0+1,x0+1)
+    float w[4];   // bilinear weights of the four corners
+    bool ok[4];   // corner inside the level
     float lx, ly;
 };
 
-__device__ __forceinline__ void bilinear_setup(const Level& L, float x, float y, long long row_stride, Corners& cr) {
+template <typename Off>
+__device__ __forceinline__ void bilinear_setup(const Level& L, float x, float y, int MD, Corners<Off>& cr) {
     // binary32 pixel coordinate, one rounding of x * W - 0.5
     const float xi = __fmaf_rn(x, L.fW, -0.5f);
     const float yi = __fmaf_rn(y, L.fH, -0.5f);
@@ -364,11 +372,11 @@ __device__ __forceinline__ void bilinear_setup(const Level& L, float x, float y,
     const bool vy1 = y0f >= -1.f && y0f < L.fH - 1.f;
     const int x0 = (vx0 || vx1) ? (int)x0f : 0;
     const int y0 = (vy0 || vy1) ? (int)y0f : 0;
-    const long long r0 = L.start + (long long)y0 * L.W + x0;
-    cr.off[0] = r0 * row_stride;
-    cr.off[1] = (r0 + 1) * row_stride;
-    cr.off[2] = (r0 + L.W) * row_stride;
-    cr.off[3] = (r0 + L.W + 1) * row_stride;
+    const Off o = (Off)L.start_md + (Off)y0 * (Off)L.w_md + (Off)x0 * (Off)MD;
+    cr.off[0] = o;
+    cr.off[1] = o + MD;
+    cr.off[2] = o + (Off)L.w_md;
+    cr.off[3] = o + (Off)L.w_md + MD;
     cr.ok[0] = vy0 && vx0;
     cr.ok[1] = vy0 && vx1;
     cr.ok[2] = vy1 && vx0;
@@ -382,59 +390,68 @@ __device__ __forceinline__ void bilinear_setup(const Level& L, float x, float y,
     cr.ly = ly;
 }
 
-template <typename T, bool SMEM>
-__device__ __forceinline__ void read_params(const KernelArgs& a, const unsigned char* sm, int team, long long u,
-                                            int s, float& x, float& y, float& w) {
-    const long long LK = a.L * a.K;
-    if constexpr (SMEM) {
-        const long long attn_off = (((long long)a.tpb * LK * 2 * (long long)sizeof(T)) + 15) & ~15ll;
-        const T* pl = reinterpret_cast<const T*>(sm) + ((long long)team * LK + s) * 2;
-        const T* pa = reinterpret_cast<const T*>(sm + attn_off) + (long long)team * LK + s;
+template <typename T>
+__device__ __forceinline__ void read_params(const KernelArgs& a, const unsigned char* sm, bool staged, int team,
+                                            uint32_t u, int s, float& x, float& y, float& w) {
+    if (staged) {
+        const T* pl = reinterpret_cast<const T*>(sm) + (team * a.LK + s) * 2;
+        const T* pa = reinterpret_cast<const T*>(sm + attn_chunk_offset<T>(a)) + team * a.LK + s;
         x = Elem<T>::to_f(pl[0]);
         y = Elem<T>::to_f(pl[1]);
         w = Elem<T>::to_f(pa[0]);
     } else {
-        const T* pl = reinterpret_cast<const T*>(a.loc) + (u * LK + s) * 2;
-        const T* pa = reinterpret_cast<const T*>(a.attn) + u * LK + s;
+        const long long ps = (long long)u * a.LK + s;
+        const T* pl = reinterpret_cast<const T*>(a.loc) + 2 * ps;
         x = ldg_f(pl);
         y = ldg_f(pl + 1);
-        w = ldg_f(pa);
+        w = ldg_f(reinterpret_cast<const T*>(a.attn) + ps);
     }
+}
+
+// Team geometry of this thread.
+struct Lane {
+    int C, P, TP, team, c, p;
+    uint32_t u0, u;
+    bool active;
+};
+__device__ __forceinline__ Lane lane_of(const KernelArgs& a) {
+    Lane r;
+    const int lcp = a.lc + a.lp;
+    r.C = 1 << a.lc;
+    r.P = 1 << a.lp;
+    r.TP = 1 << lcp;
+    r.team = threadIdx.x >> lcp;
+    const int lt = threadIdx.x & (r.TP - 1);
+    r.c = lt & (r.C - 1);
+    r.p = lt >> a.lc;
+    r.u0 = blockIdx.x * (uint32_t)a.tpb;
+    r.u = r.u0 + r.team;
+    r.active = r.u < (uint32_t)a.n_units;
+    return r;
 }
 
 // ---------------------------------------------------------------------------
 // forward (course ch. 4; README "Kernel design" item 1)
 
-template <typename T, int NV, int EPV, bool SMEM, int U>
+template <typename T, int NV, int EPV, bool WIDE, int U>
 __global__ void __launch_bounds__(kBlockThreads) msda_fwd_kernel(const KernelArgs a) {
+    using Off = typename std::conditional<WIDE, long long, int>::type;
+    using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
+    __shared__ int verdict;
     extern __shared__ __align__(16) unsigned char sm[];
 
-    const int lcp = a.lc + a.lp;
-    const int C = 1 << a.lc, P = 1 << a.lp, TP = 1 << lcp;
-    const int team = threadIdx.x >> lcp;
-    const int lt = threadIdx.x & (TP - 1);
-    const int c = lt & (C - 1);
-    const int p = lt >> a.lc;
-    const int LK = (int)(a.L * a.K);
-    const long long u0 = (long long)blockIdx.x * a.tpb;
-    const long long u = u0 + team;
-    const bool active = u < a.n_units;
-
-    load_levels(a, lv);
-    if constexpr (SMEM) {
-        if (!stage_params<T>(a, sm, u0, &bar)) {
-            if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
-            return;  // nothing was written; the host reports the error bit
-        }
+    const Lane ln = lane_of(a);
+    if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
+        if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
+        return;  // nothing was written; the host reports the error bit
     }
-    __syncthreads();
-
-    const long long b = active ? u / (a.Q * a.M) : 0;
-    const long long m = active ? u % a.M : 0;
-    const long long row_stride = a.M * a.D;
-    const T* vbase = reinterpret_cast<const T*>(a.value) + (b * a.S * a.M + m) * a.D;
+    const bool staged = a.param_mode != PARAMS_DIRECT;
+    const uint32_t b = fdiv(ln.u, a.div_qm);
+    const uint32_t m = ln.u - fdiv(ln.u, a.div_m) * (uint32_t)a.M;
+    const T* vbase = reinterpret_cast<const T*>(a.value) + (long long)b * a.slice + (long long)m * a.D;
+    const int MD = a.M * a.D;
 
     float acc[NV][EPV];
 #pragma unroll
@@ -442,33 +459,30 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd_kernel(const KernelArg
 #pragma unroll
         for (int e = 0; e < EPV; ++e) acc[n][e] = 0.f;
 
-    using S_ = Slot<T, EPV>;
-    for (int s0 = 0; s0 < LK; s0 += P * U) {
+    for (int s0 = 0; s0 < a.LK; s0 += ln.P * U) {
         typename S_::Raw vals[U][4][NV];
         float coef[U][4];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-            const int s = s0 + p + i * P;
-            Corners cr;
+            const int s = s0 + ln.p + i * ln.P;
+            const bool live = ln.active && s < a.LK;
             float x = -4.f, y = -4.f, w = 0.f;
             int l = 0;
-            if (active && s < LK) {
-                read_params<T, SMEM>(a, sm, team, u, s, x, y, w);
-                l = s / (int)a.K;
-            } else {
-                l = 0;
+            if (live) {
+                read_params<T>(a, sm, staged, ln.team, ln.u, s, x, y, w);
+                l = (int)fdiv((uint32_t)s, a.div_k);
             }
             Level lev = lv[l];
-            if (!(active && s < LK)) lev.ok = 0;
-            bilinear_setup(lev, x, y, row_stride, cr);
+            if (!live) lev.ok = 0;
+            Corners<Off> cr;
+            bilinear_setup<Off>(lev, x, y, MD, cr);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 coef[i][k] = cr.ok[k] ? w * cr.w[k] : 0.f;
 #pragma unroll
                 for (int n = 0; n < NV; ++n) {
-                    const int j = n * C + c;
-                    vals[i][k][n] = (cr.ok[k] && j < a.nvec) ? S_::load_raw(vbase + cr.off[k] + (long long)j * EPV)
-                                                             : S_::zero();
+                    const int j = n * ln.C + ln.c;
+                    vals[i][k][n] = (cr.ok[k] && j < a.nvec) ? S_::load_raw(vbase + cr.off[k] + j * EPV) : S_::zero();
                 }
             }
         }
@@ -486,18 +500,18 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd_kernel(const KernelArg
     }
 
     // combine the P point lanes of the team
-    for (int o = C; o < TP; o <<= 1) {
+    for (int o = ln.C; o < ln.TP; o <<= 1) {
 #pragma unroll
         for (int n = 0; n < NV; ++n)
 #pragma unroll
             for (int e = 0; e < EPV; ++e) acc[n][e] += __shfl_xor_sync(0xffffffffu, acc[n][e], o);
     }
-    if (active && p == 0) {
-        T* o = reinterpret_cast<T*>(a.out) + u * a.D;
+    if (ln.active && ln.p == 0) {
+        T* o = reinterpret_cast<T*>(a.out) + (long long)ln.u * a.D;
 #pragma unroll
         for (int n = 0; n < NV; ++n) {
-            const int j = n * C + c;
-            if (j < a.nvec) Slot<T, EPV>::store(o + (long long)j * EPV, acc[n]);
+            const int j = n * ln.C + ln.c;
+            if (j < a.nvec) S_::store(o + j * EPV, acc[n]);
         }
     }
 }
@@ -505,46 +519,35 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd_kernel(const KernelArg
 // ---------------------------------------------------------------------------
 // backward (course ch. 5; README "Kernel design" items 2, 3)
 
-template <typename T, typename ACC, int NV, int EPV, bool SMEM, int U>
+template <typename T, typename ACC, int NV, int EPV, bool WIDE, int U>
 __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArgs a) {
+    using Off = typename std::conditional<WIDE, long long, int>::type;
+    using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
+    __shared__ int verdict;
     extern __shared__ __align__(16) unsigned char sm[];
 
-    const int lcp = a.lc + a.lp;
-    const int C = 1 << a.lc, P = 1 << a.lp, TP = 1 << lcp;
-    const int team = threadIdx.x >> lcp;
-    const int lt = threadIdx.x & (TP - 1);
-    const int c = lt & (C - 1);
-    const int p = lt >> a.lc;
-    const int LK = (int)(a.L * a.K);
-    const long long u0 = (long long)blockIdx.x * a.tpb;
-    const long long u = u0 + team;
-    const bool active = u < a.n_units;
-
-    load_levels(a, lv);
-    if constexpr (SMEM) {
-        if (!stage_params<T>(a, sm, u0, &bar)) {
-            if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
-            return;
-        }
+    const Lane ln = lane_of(a);
+    if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
+        if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
+        return;
     }
-    __syncthreads();
-
-    const long long b = active ? u / (a.Q * a.M) : 0;
-    const long long m = active ? u % a.M : 0;
-    const long long row_stride = a.M * a.D;
-    const long long vofs = (b * a.S * a.M + m) * a.D;
+    const bool staged = a.param_mode != PARAMS_DIRECT;
+    const uint32_t b = fdiv(ln.u, a.div_qm);
+    const uint32_t m = ln.u - fdiv(ln.u, a.div_m) * (uint32_t)a.M;
+    const long long vofs = (long long)b * a.slice + (long long)m * a.D;
     const T* vbase = reinterpret_cast<const T*>(a.value) + vofs;
     ACC* gbase = reinterpret_cast<ACC*>(a.grad_acc) + vofs;
+    const int MD = a.M * a.D;
 
     // this lane's slots of g = grad_out[b, q, m, :]
     float g[NV][EPV];
 #pragma unroll
     for (int n = 0; n < NV; ++n) {
-        const int j = n * C + c;
-        if (active && j < a.nvec) {
-            Slot<T, EPV>::load(reinterpret_cast<const T*>(a.grad_out) + u * a.D + (long long)j * EPV, g[n]);
+        const int j = n * ln.C + ln.c;
+        if (ln.active && j < a.nvec) {
+            S_::load(reinterpret_cast<const T*>(a.grad_out) + (long long)ln.u * a.D + j * EPV, g[n]);
         } else {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) g[n][e] = 0.f;
@@ -554,26 +557,24 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
     T* gl = reinterpret_cast<T*>(a.grad_loc);
     T* ga = reinterpret_cast<T*>(a.grad_attn);
 
-    using S_ = Slot<T, EPV>;
-    for (int s0 = 0; s0 < LK; s0 += P * U) {
+    for (int s0 = 0; s0 < a.LK; s0 += ln.P * U) {
         typename S_::Raw vals[U][4][NV];
-        Corners cr[U];
-        float wa[U];
+        Corners<Off> cr[U];
+        float wa[U], fW[U], fH[U];
         bool live[U];
-        float fW[U], fH[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-            const int s = s0 + p + i * P;
+            const int s = s0 + ln.p + i * ln.P;
+            live[i] = ln.active && s < a.LK;
             float x = -4.f, y = -4.f, w = 0.f;
             int l = 0;
-            live[i] = active && s < LK;
             if (live[i]) {
-                read_params<T, SMEM>(a, sm, team, u, s, x, y, w);
-                l = s / (int)a.K;
+                read_params<T>(a, sm, staged, ln.team, ln.u, s, x, y, w);
+                l = (int)fdiv((uint32_t)s, a.div_k);
             }
             Level lev = lv[l];
             if (!live[i]) lev.ok = 0;
-            bilinear_setup(lev, x, y, row_stride, cr[i]);
+            bilinear_setup<Off>(lev, x, y, MD, cr[i]);
             wa[i] = w;
             fW[i] = lev.fW;
             fH[i] = lev.fH;
@@ -581,10 +582,9 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
             for (int k = 0; k < 4; ++k)
 #pragma unroll
                 for (int n = 0; n < NV; ++n) {
-                    const int j = n * C + c;
-                    vals[i][k][n] = (cr[i].ok[k] && j < a.nvec)
-                                        ? S_::load_raw(vbase + cr[i].off[k] + (long long)j * EPV)
-                                        : S_::zero();
+                    const int j = n * ln.C + ln.c;
+                    vals[i][k][n] = (cr[i].ok[k] && j < a.nvec) ? S_::load_raw(vbase + cr[i].off[k] + j * EPV)
+                                                                : S_::zero();
                 }
         }
 #pragma unroll
@@ -609,14 +609,14 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
             float r_a = any ? (cr[i].w[0] * d[0] + cr[i].w[1] * d[1] + cr[i].w[2] * d[2] + cr[i].w[3] * d[3]) : 0.f;
             float r_x = any ? ((1.f - ly) * (d[1] - d[0]) + ly * (d[3] - d[2])) : 0.f;
             float r_y = any ? ((1.f - lx) * (d[2] - d[0]) + lx * (d[3] - d[1])) : 0.f;
-            for (int o = 1; o < C; o <<= 1) {
+            for (int o = 1; o < ln.C; o <<= 1) {
                 r_a += __shfl_xor_sync(0xffffffffu, r_a, o);
                 r_x += __shfl_xor_sync(0xffffffffu, r_x, o);
                 r_y += __shfl_xor_sync(0xffffffffu, r_y, o);
             }
-            const int s = s0 + p + i * P;
-            if (live[i] && c == 0) {
-                const long long ps = u * LK + s;
+            const int s = s0 + ln.p + i * ln.P;
+            if (live[i] && ln.c == 0) {
+                const long long ps = (long long)ln.u * a.LK + s;
                 ga[ps] = Elem<T>::from_f(r_a);
                 gl[2 * ps] = Elem<T>::from_f(wa[i] * fW[i] * r_x);
                 gl[2 * ps + 1] = Elem<T>::from_f(wa[i] * fH[i] * r_y);
@@ -628,12 +628,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
                 const float cf = wa[i] * cr[i].w[k];
 #pragma unroll
                 for (int n = 0; n < NV; ++n) {
-                    const int j = n * C + c;
+                    const int j = n * ln.C + ln.c;
                     if (j < a.nvec) {
                         float t[EPV];
 #pragma unroll
                         for (int e = 0; e < EPV; ++e) t[e] = cf * g[n][e];
-                        Scatter<ACC, EPV>::add(gbase + cr[i].off[k] + (long long)j * EPV, t);
+                        Scatter<ACC, EPV>::add(gbase + cr[i].off[k] + j * EPV, t);
                     }
                 }
             }

@@ -16,7 +16,7 @@ struct Plan {
     size_t smem;   // dynamic shared memory (staged parameters)
     int nv;        // vectors per lane, 1..4
     bool vec;      // 16-byte slots (else one element per slot)
-    bool smem_params;
+    bool wide;     // 64-bit offsets inside a batch slice
 };
 
 #define MSDA_DISPATCH_NV(NVV, ...)                                   \
@@ -27,24 +27,24 @@ struct Plan {
     default: { constexpr int NV = 4; __VA_ARGS__; } break;           \
     }
 
-template <typename T, int NV, int EPV, bool SM>
+template <typename T, int NV, int EPV, bool WIDE>
 static void fwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
-    msda_fwd_kernel<T, NV, EPV, SM, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
+    msda_fwd_kernel<T, NV, EPV, WIDE, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
 }
 
-template <typename T, typename ACC, int NV, int EPV, bool SM>
+template <typename T, typename ACC, int NV, int EPV, bool WIDE>
 static void bwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
-    msda_bwd_kernel<T, ACC, NV, EPV, SM, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
+    msda_bwd_kernel<T, ACC, NV, EPV, WIDE, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
 }
 
 template <typename T>
 void launch_forward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     constexpr int VE = 16 / sizeof(T);
     if (pl.vec) {
-        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, true>(a, pl, st))) }
+        if (pl.wide) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, true>(a, pl, st))) }
         else { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, false>(a, pl, st))) }
     } else {
-        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, 1, true>(a, pl, st))) }
+        if (pl.wide) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, 1, true>(a, pl, st))) }
         else { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, 1, false>(a, pl, st))) }
     }
 }
@@ -53,10 +53,10 @@ template <typename T, typename ACC>
 void launch_backward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     constexpr int VE = 16 / sizeof(T);
     if (pl.vec) {
-        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, true>(a, pl, st))) }
+        if (pl.wide) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, true>(a, pl, st))) }
         else { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, false>(a, pl, st))) }
     } else {
-        if (pl.smem_params) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, 1, true>(a, pl, st))) }
+        if (pl.wide) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, 1, true>(a, pl, st))) }
         else { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, 1, false>(a, pl, st))) }
     }
 }

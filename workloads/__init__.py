@@ -83,7 +83,7 @@ WORKLOADS: Dict[str, Workload] = {
                           dtype="f32", loc="uniform_wide", logits="normal", seed=0),
     # decoder cross-attention: 300 object queries per image
     "decoder_bf16": Workload("decoder_bf16", B=4, M=8, D=32, K=4, shapes=_PYRAMID_800x1333, Q=300,
-                             dtype="bf16", loc="uniform01", logits="uniform01", seed=1, accum="fp32"),
+                             dtype="bf16", loc="uniform01", logits="uniform01", seed=1),
     # encoder self-attention: every pyramid pixel is a query
     "encoder_fp16": Workload("encoder_fp16", B=2, M=8, D=32, K=4, shapes=_PYRAMID_800x1333, Q=None,
                              dtype="f16", loc="pixel_centres", logits="normal", seed=2),
