@@ -248,13 +248,35 @@ class GpuStep:
         return [a.elapsed_time(b) for a, b in ev]
 
 
-def _dist():
+def _dist(backend: str = "nccl"):
     import torch.distributed as dist
 
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
     return dist if ws > 1 else None, int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def rank_workload(wl: W.Workload, rank: int) -> W.Workload:
+    """Weak scaling: every rank runs the same sizes on its own seeded batch
+    (the path shards over batches; no data-path exchange exists)."""
+    return wl.with_(seed=wl.seed + 1000 * rank) if rank else wl
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time (barrier-bracketed timings are reduced by MAX)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job (b, q, m) outputs per second: all ranks' units over the max time."""
+    return units_per_rank * world * steps / (total_ms / 1e3)
 
 
 def run_ours(args):
@@ -265,8 +287,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     import scale_deformable_attention_gb300 as msda
 
-    wl = W.WORKLOADS[args.workload]
-    wl = wl.with_(seed=wl.seed + 1000 * rank) if rank else wl
+    wl = rank_workload(W.WORKLOADS[args.workload], rank)
     inp = W.make_inputs(wl)
     accum = args.accum or wl.accum
     st = GpuStep(wl, inp, accum, device)
@@ -294,13 +315,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     recs, dropped = msda.trace_read()
     msda.trace_enable(0)
-    total_ms = float(sum(times))
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(sum(times)), dist, device)
     ms_per_step = total_ms / args.steps
-    value = wl.units * world * args.steps / (total_ms / 1e3)
+    value = job_throughput(wl.units, world, args.steps, total_ms)
 
     # per-kernel durations over the traced part of the timed region
     per = {}
