@@ -153,6 +153,31 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
                           void* grad_value, void* grad_sampling_locations, void* grad_attention_weights,
                           void* workspace, size_t workspace_bytes, msda_stream_t stream);
 
+/*
+ * Backward with the FP32 accumulator whose scratch lives in a fixed device
+ * array inside the library instead of a caller-provided workspace; it
+ * allocates nothing.  The pages have no counterpart: this is for callers that
+ * can pass input and output buffers but cannot allocate device memory when
+ * they call (an engine plugin handed only its tensors, a loop that forbids
+ * allocation after start-up).  Results equal msda_backward(dt,
+ * MSDA_ACCUM_FP32, flags, ...) up to the summation order of grad_value.
+ *
+ * Limit: B*S*M*D <= MSDA_STATIC_WORKSPACE_BYTES / 4 for fp16 / bf16, else
+ * MSDA_ERR_WORKSPACE before anything is enqueued (fp32 I/O needs no scratch
+ * and has no limit).  Every GPU on which it is called holds the array until
+ * the process exits.  The first call on a device looks up the array's device
+ * address; make it before any stream capture.  All calls share the one
+ * array: calls that can overlap on the GPU race and must be serialised by the
+ * caller.  Other arguments and errors as msda_backward.
+ */
+#define MSDA_STATIC_WORKSPACE_BYTES (64u << 20)
+msda_status msda_backward_static_workspace(msda_dtype dt, unsigned flags, int64_t B, int64_t S, int64_t M, int64_t D,
+                                           int64_t L, int64_t K, int64_t Q, const void* value,
+                                           const int64_t* spatial_shapes, const int64_t* level_start_index,
+                                           const void* sampling_locations, const void* attention_weights,
+                                           const void* grad_out, void* grad_value, void* grad_sampling_locations,
+                                           void* grad_attention_weights, msda_stream_t stream);
+
 /* Message for the last non-OK status returned on the calling thread ("" if none). */
 const char* msda_last_error(void);
 

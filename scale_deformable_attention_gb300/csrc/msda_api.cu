@@ -11,6 +11,7 @@
 #include <mutex>
 #include <vector>
 
+#include "msda_internal.h"
 #include "msda_launch.cuh"
 
 using msda::KernelArgs;
@@ -311,6 +312,10 @@ msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
     return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "zero kernel launch");
 }
 }  // namespace
+
+namespace msda {
+msda_status set_error(msda_status s, const char* message) { return fail(s, "%s", message); }
+}  // namespace msda
 
 // ---------------------------------------------------------------------------
 // C ABI
