@@ -235,15 +235,22 @@ class GpuStep:
         # writing back someone else's dirty lines
         self.flush_sink = self.flush_buf.sum()
 
-    def timed(self, fn, steps: int):
-        """Device time of `fn` per step with the L2 flushed before each one (ms)."""
+    def timed(self, fn, steps: int, trace_every: int = 0):
+        """Device time of `fn` per step with the L2 flushed before each one (ms).
+        With trace_every = n > 0 the library's kernel trace records every n-th
+        step only (its event pairs serialise the kernels of the step they
+        bracket, so tracing every step would slow the step being measured)."""
         torch = self.torch
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for a, b in ev:
+        for i, (a, b) in enumerate(ev):
+            if trace_every:
+                self.msda.trace_pause(i % trace_every != 0)
             self.flush()
             a.record()
             fn()
             b.record()
+        if trace_every:
+            self.msda.trace_pause(False)
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in ev]
 
@@ -304,14 +311,14 @@ def run_ours(args):
     recs, _ = msda.trace_read()
     launches_per_step = len(recs)
 
-    msda.trace_enable(min(4 * args.steps + 8, 16384))
+    msda.trace_enable(4 * (args.steps // args.trace_every + 2))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     with ClockSampler(uuid) as clk:
-        times = st.timed(st.step, args.steps)
+        times = st.timed(st.step, args.steps, trace_every=args.trace_every)
     torch.cuda.synchronize()
     recs, dropped = msda.trace_read()
     msda.trace_enable(0)
@@ -353,7 +360,7 @@ def run_ours(args):
             "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
             "roofline": roof, "kernels": kernels, "bytes_per_step_model": model["step"],
             "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
-            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped,
+            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "traced_steps_every": args.trace_every,
         }
         print(json.dumps(line), flush=True)
     if args.all and rank == 0:
@@ -513,6 +520,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--trace-every", type=int, default=16,
+                    help="record per-kernel events on every n-th timed step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
     args = ap.parse_args(argv)

@@ -211,6 +211,9 @@ enum { MSDA_KERNEL_FORWARD = 0, MSDA_KERNEL_BACKWARD = 1, MSDA_KERNEL_ZERO = 2, 
        MSDA_KERNEL_COUNT = 4 };
 
 msda_status msda_trace_enable(int capacity);
+/* Pause (paused != 0) or resume recording without destroying the events:
+ * a paused trace adds no work to the streams. */
+void msda_trace_pause(int paused);
 int msda_trace_read(msda_trace_record* records, int max_records, int* dropped);
 const char* msda_kernel_name(int kernel);
 

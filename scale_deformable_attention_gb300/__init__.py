@@ -27,7 +27,7 @@ from . import _lib
 from ._lib import ACCUM, BWD_ACCUMULATE, MsdaError
 
 __all__ = ["multi_scale_deformable_attention", "forward", "backward", "workspace_size", "resolve_accum",
-           "device_errors", "trace_enable", "trace_read", "MsdaError", "DTYPE_CODE"]
+           "device_errors", "trace_enable", "trace_pause", "trace_read", "MsdaError", "DTYPE_CODE"]
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
@@ -204,6 +204,11 @@ def device_errors(clear: bool = True) -> int:
 def trace_enable(capacity: int) -> None:
     """Bracket every kernel launch by CUDA events (capacity launches; 0 disables)."""
     _lib.check(_lib.lib().msda_trace_enable(int(capacity)))
+
+
+def trace_pause(paused: bool) -> None:
+    """Stop (or resume) recording launches without destroying the trace's events."""
+    _lib.lib().msda_trace_pause(1 if paused else 0)
 
 
 def trace_read(max_records: int = 1 << 16):

@@ -10,7 +10,8 @@ import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libmsda.so")
+# MSDA_LIBRARY points the binding at another build of the same library
+LIB_PATH = os.environ.get("MSDA_LIBRARY") or os.path.join(PKG, "libmsda.so")
 
 MSDA_OK = 0
 STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTED", 3: "MSDA_ERR_MISALIGNED",
@@ -56,6 +57,8 @@ def _declare(lib):
     lib.msda_version.restype = c_int
     lib.msda_trace_enable.argtypes = [c_int]
     lib.msda_trace_enable.restype = c_int
+    lib.msda_trace_pause.argtypes = [c_int]
+    lib.msda_trace_pause.restype = None
     lib.msda_trace_read.argtypes = [ctypes.POINTER(TraceRecord), c_int, ctypes.POINTER(c_int)]
     lib.msda_trace_read.restype = c_int
     lib.msda_kernel_name.argtypes = [c_int]

@@ -84,6 +84,7 @@ msda_status device_info(DeviceInfo** out) {
 
 struct Trace {
     int cap = 0, n = 0, dropped = 0, device = -1;
+    bool paused = false;
     std::vector<cudaEvent_t> ev;
     std::vector<int> kernel;
     std::vector<int64_t> work;
@@ -91,11 +92,16 @@ struct Trace {
 Trace g_trace;
 std::mutex g_trace_mu;
 
+bool trace_active() {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    return g_trace.cap > 0 && !g_trace.paused;
+}
+
 struct TraceScope {
     int slot = -1;
     cudaStream_t st;
     TraceScope(cudaStream_t s) : st(s) {
-        if (g_trace.cap == 0) return;
+        if (g_trace.cap == 0 || g_trace.paused) return;
         std::lock_guard<std::mutex> lk(g_trace_mu);
         if (g_trace.n >= g_trace.cap) {
             ++g_trace.dropped;
@@ -116,6 +122,7 @@ struct TraceScope {
 
 struct Tune {
     int C = 0, P = 0, params = -1;
+    bool generic = false;  // force the generic kernels
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -130,6 +137,7 @@ const Tune& tune() {
             else if (!strcmp(tok, "params=bulk")) r.params = msda::PARAMS_SMEM_BULK;
             else if (!strcmp(tok, "params=ld")) r.params = msda::PARAMS_SMEM_LD;
             else if (!strcmp(tok, "params=direct")) r.params = msda::PARAMS_DIRECT;
+            else if (!strcmp(tok, "generic")) r.generic = true;
         }
         return r;
     }();
@@ -271,6 +279,8 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     pl.wide = a.slice > (1ll << 30);
     pl.nv = NV;
     pl.vec = vec;
+    pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && NV <= 3 && !t.generic;
+    pl.pdl = false;
     return MSDA_OK;
 }
 
@@ -287,6 +297,9 @@ int grid_for(int64_t n, int sms) {
 
 namespace msda {
 __global__ void __launch_bounds__(kBlockThreads) msda_zero_kernel(unsigned char* p, long long nbytes) {
+    // a backward launched as a programmatic dependent may start its gather
+    // phase now; it waits for this grid before its first scatter
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // head up to 16-byte alignment, 16-byte body, tail
     const uintptr_t addr = reinterpret_cast<uintptr_t>(p);
     const long long head = min((long long)((16 - (addr & 15)) & 15), nbytes);
@@ -305,8 +318,11 @@ namespace {
 msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
     if (nbytes <= 0) return MSDA_OK;
     TraceScope ts(st);
-    msda::msda_zero_kernel<<<grid_for(nbytes / 16 + 1, sms), msda::kBlockThreads, 0, st>>>(
-        static_cast<unsigned char*>(p), nbytes);
+    // two blocks per SM: stores need no registers in flight, and the rest of
+    // the SM stays free for a backward that starts early (programmatic launch)
+    const int64_t want = nbytes / 16 / msda::kBlockThreads + 1;
+    const int grid = (int)(want < 2 * (int64_t)sms ? want : 2 * (int64_t)sms);
+    msda::msda_zero_kernel<<<grid, msda::kBlockThreads, 0, st>>>(static_cast<unsigned char*>(p), nbytes);
     ts.end(MSDA_KERNEL_ZERO, nbytes);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "zero kernel launch");
@@ -474,6 +490,10 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
         if (e != cudaSuccess) return cuda_fail(e, "widen kernel launch");
     }
 
+    // the zero kernel was the last thing enqueued by this call: the backward
+    // may be launched as its programmatic dependent (not while tracing, whose
+    // events sit between the two launches)
+    const bool zeroed_here = !accumulate && (use_ws || d.n_value > 0);
     void* acc_buf = use_ws ? workspace : grad_value;
     const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16) &&
                      aligned(acc_buf, 16);
@@ -490,6 +510,7 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
     a.grad_loc = grad_sampling_locations;
     a.grad_attn = grad_attention_weights;
     a.err = di->err;
+    pl.pdl = pl.spec && zeroed_here && !trace_active();
     {
         TraceScope ts(st);
         switch (dt) {
@@ -565,6 +586,11 @@ msda_status msda_trace_enable(int capacity) {
     g_trace.work.assign(capacity, 0);
     g_trace.cap = capacity;
     return MSDA_OK;
+}
+
+void msda_trace_pause(int paused) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    g_trace.paused = paused != 0;
 }
 
 int msda_trace_read(msda_trace_record* records, int max_records, int* dropped) {

@@ -642,6 +642,332 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
 }
 
 // ---------------------------------------------------------------------------
+// Specialised kernels for rows of whole 16-byte vectors: C = 4 channel lanes
+// with NV vectors each (D = 32 * NV bf16/fp16 or 16 * NV fp32 channels),
+// 32-bit slice offsets, runtime P.
+//
+// One bilinear setup per sample.  The samples of a unit are taken in rounds
+// of 4P; in a round starting at r0 the lane (c, p) of a team sets up sample
+// r0 + p + c*P, and the four channel lanes of point group p take it in turn
+// (iteration j uses the setup of lane (j, p)), reading it with warp shuffles
+// instead of recomputing it.  The producer lane also writes that sample's
+// grad_attn / grad_loc, since it holds the level sizes and the weight.
+
+constexpr int kC = 4;
+
+struct SampleSetup {
+    int o;          // element offset of corner (y0, x0) in the slice
+    int wmd;        // W * M * D of the sample's level
+    unsigned mask;  // bit k: corner k inside the level
+    float lx, ly;   // fractional offsets in the cell
+};
+
+__device__ __forceinline__ SampleSetup sample_setup(const Level& L, float x, float y, int MD) {
+    // binary32 pixel coordinate, one rounding of x * W - 0.5 (as bilinear_setup)
+    const float xi = __fmaf_rn(x, L.fW, -0.5f);
+    const float yi = __fmaf_rn(y, L.fH, -0.5f);
+    const float x0f = floorf(xi), y0f = floorf(yi);
+    const bool vx0 = L.ok && x0f >= 0.f && x0f < L.fW;
+    const bool vx1 = L.ok && x0f >= -1.f && x0f < L.fW - 1.f;
+    const bool vy0 = y0f >= 0.f && y0f < L.fH;
+    const bool vy1 = y0f >= -1.f && y0f < L.fH - 1.f;
+    const int x0 = (vx0 || vx1) ? (int)x0f : 0;
+    const int y0 = (vy0 || vy1) ? (int)y0f : 0;
+    SampleSetup r;
+    r.wmd = (int)L.w_md;
+    r.o = (int)L.start_md + y0 * r.wmd + x0 * MD;
+    r.mask = (unsigned)(vy0 && vx0) | ((unsigned)(vy0 && vx1) << 1) | ((unsigned)(vy1 && vx0) << 2) |
+             ((unsigned)(vy1 && vx1) << 3);
+    r.lx = xi - x0f;
+    r.ly = yi - y0f;
+    return r;
+}
+
+__device__ __forceinline__ SampleSetup shfl_setup(const SampleSetup& s, int src) {
+    SampleSetup r;
+    r.o = __shfl_sync(0xffffffffu, s.o, src);
+    r.wmd = __shfl_sync(0xffffffffu, s.wmd, src);
+    r.mask = __shfl_sync(0xffffffffu, s.mask, src);
+    r.lx = __shfl_sync(0xffffffffu, s.lx, src);
+    r.ly = __shfl_sync(0xffffffffu, s.ly, src);
+    return r;
+}
+
+// bilinear weights of the four corners
+__device__ __forceinline__ void corner_weights(float lx, float ly, float (&w)[4]) {
+    const float hx = 1.f - lx, hy = 1.f - ly;
+    w[0] = hx * hy;
+    w[1] = lx * hy;
+    w[2] = hx * ly;
+    w[3] = lx * ly;
+}
+
+// acc[e] += c * v[e] on pairs of lanes with the packed fp32x2 FMA
+template <int EPV>
+__device__ __forceinline__ void axpy2(float (&acc)[EPV], float c, const float (&v)[EPV]) {
+    const float2 cc = make_float2(c, c);
+#pragma unroll
+    for (int e = 0; e < EPV; e += 2) {
+        float2 r = __ffma2_rn(cc, make_float2(v[e], v[e + 1]), make_float2(acc[e], acc[e + 1]));
+        acc[e] = r.x;
+        acc[e + 1] = r.y;
+    }
+}
+
+// sum over e of g[e] * v[e], pairwise then folded
+template <int EPV>
+__device__ __forceinline__ float dot2(const float (&g)[EPV], const float (&v)[EPV]) {
+    float2 t = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < EPV; e += 2) t = __ffma2_rn(make_float2(g[e], g[e + 1]), make_float2(v[e], v[e + 1]), t);
+    return t.x + t.y;
+}
+
+// Lane index (within the warp) of lane (c, p) of this thread's team.
+__device__ __forceinline__ int team_lane(const Lane& ln, int c, int p) {
+    return ((threadIdx.x & 31) & ~(ln.TP - 1)) + c + p * kC;
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelArgs a) {
+    constexpr int EPV = 16 / sizeof(T);
+    using S_ = Slot<T, EPV>;
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int verdict;
+    extern __shared__ __align__(16) unsigned char sm[];
+
+    const Lane ln = lane_of(a);
+    if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
+        if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
+        return;
+    }
+    const bool staged = a.param_mode != PARAMS_DIRECT;
+    const uint32_t b = fdiv(ln.u, a.div_qm);
+    const uint32_t m = ln.u - fdiv(ln.u, a.div_m) * (uint32_t)a.M;
+    const T* vbase = reinterpret_cast<const T*>(a.value) + (long long)b * a.slice + (long long)m * a.D + ln.c * EPV;
+    const int MD = a.M * a.D;
+
+    float acc[NV][EPV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[n][e] = 0.f;
+
+    for (int r0 = 0; r0 < a.LK; r0 += ln.TP) {
+        // this lane's sample of the round
+        const int s_own = r0 + ln.p + ln.c * ln.P;
+        const bool live = ln.active && s_own < a.LK;
+        float x = -4.f, y = -4.f, w = 0.f;
+        int l = 0;
+        if (live) {
+            read_params<T>(a, sm, staged, ln.team, ln.u, s_own, x, y, w);
+            l = (int)fdiv((uint32_t)s_own, a.div_k);
+        }
+        Level lev = lv[l];
+        if (!live) lev.ok = 0;
+        SampleSetup me = sample_setup(lev, x, y, MD);
+        float mw[4];
+        corner_weights(me.lx, me.ly, mw);
+        float mc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mc[k] = ((me.mask >> k) & 1u) ? w * mw[k] : 0.f;
+
+#pragma unroll
+        for (int j0 = 0; j0 < kC; j0 += 2) {
+            typename S_::Raw raw[2][4][NV];
+            float cf[2][4];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int src = team_lane(ln, j0 + jj, ln.p);
+                const int o = __shfl_sync(0xffffffffu, me.o, src);
+                const int wmd = __shfl_sync(0xffffffffu, me.wmd, src);
+                const unsigned mask = __shfl_sync(0xffffffffu, me.mask, src);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cf[jj][k] = __shfl_sync(0xffffffffu, mc[k], src);
+                const int off[4] = {o, o + MD, o + wmd, o + wmd + MD};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int n = 0; n < NV; ++n)
+                        raw[jj][k][n] = ((mask >> k) & 1u) ? S_::load_raw(vbase + off[k] + n * kC * EPV) : S_::zero();
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) {
+                        float v[EPV];
+                        S_::unpack(raw[jj][k][n], v);
+                        axpy2(acc[n], cf[jj][k], v);
+                    }
+        }
+    }
+
+    // combine the P point lanes of the team
+    for (int o = kC; o < ln.TP; o <<= 1) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[n][e] += __shfl_xor_sync(0xffffffffu, acc[n][e], o);
+    }
+    if (ln.active && ln.p == 0) {
+        T* o = reinterpret_cast<T*>(a.out) + (long long)ln.u * a.D + ln.c * EPV;
+#pragma unroll
+        for (int n = 0; n < NV; ++n) S_::store(o + n * kC * EPV, acc[n]);
+    }
+}
+
+// Backward, same decomposition.  Each round first gathers the corners of its
+// samples and reduces <g, corner> to grad_attn / grad_loc (reads only), then
+// scatters grad_value.  When launched as a programmatic dependent of the
+// zero kernel, griddepcontrol.wait before the first scatter lets the gather
+// phase of the first round overlap the zeroing of grad_value; launched
+// normally, the wait returns at once.
+template <typename T, typename ACC, int NV>
+__global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
+    constexpr int EPV = 16 / sizeof(T);
+    using S_ = Slot<T, EPV>;
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int verdict;
+    extern __shared__ __align__(16) unsigned char sm[];
+
+    const Lane ln = lane_of(a);
+    if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
+        if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
+        return;
+    }
+    const bool staged = a.param_mode != PARAMS_DIRECT;
+    const uint32_t b = fdiv(ln.u, a.div_qm);
+    const uint32_t m = ln.u - fdiv(ln.u, a.div_m) * (uint32_t)a.M;
+    const long long vofs = (long long)b * a.slice + (long long)m * a.D + ln.c * EPV;
+    const T* vbase = reinterpret_cast<const T*>(a.value) + vofs;
+    ACC* gbase = reinterpret_cast<ACC*>(a.grad_acc) + vofs;
+    const int MD = a.M * a.D;
+
+    // this lane's channel slots of g = grad_out[b, q, m, :]
+    float g[NV][EPV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+        if (ln.active) {
+            S_::load(reinterpret_cast<const T*>(a.grad_out) + (long long)ln.u * a.D + ln.c * EPV + n * kC * EPV, g[n]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) g[n][e] = 0.f;
+        }
+    }
+    T* gl = reinterpret_cast<T*>(a.grad_loc);
+    T* ga = reinterpret_cast<T*>(a.grad_attn);
+    bool waited = false;
+
+    for (int r0 = 0; r0 < a.LK; r0 += ln.TP) {
+        const int s_own = r0 + ln.p + ln.c * ln.P;
+        const bool live = ln.active && s_own < a.LK;
+        float x = -4.f, y = -4.f, wa = 0.f;
+        int l = 0;
+        if (live) {
+            read_params<T>(a, sm, staged, ln.team, ln.u, s_own, x, y, wa);
+            l = (int)fdiv((uint32_t)s_own, a.div_k);
+        }
+        Level lev = lv[l];
+        if (!live) lev.ok = 0;
+        const SampleSetup me = sample_setup(lev, x, y, MD);
+
+        // gather + reduce: the lane with c == j keeps the totals of sample j
+        float ra = 0.f, rx = 0.f, ry = 0.f;
+#pragma unroll
+        for (int j0 = 0; j0 < kC; j0 += 2) {
+            typename S_::Raw raw[2][4][NV];
+            SampleSetup st[2];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                st[jj] = shfl_setup(me, team_lane(ln, j0 + jj, ln.p));
+                const int off[4] = {st[jj].o, st[jj].o + MD, st[jj].o + st[jj].wmd, st[jj].o + st[jj].wmd + MD};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int n = 0; n < NV; ++n)
+                        raw[jj][k][n] = ((st[jj].mask >> k) & 1u) ? S_::load_raw(vbase + off[k] + n * kC * EPV)
+                                                                  : S_::zero();
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                float d[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float t = 0.f;
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) {
+                        float v[EPV];
+                        S_::unpack(raw[jj][k][n], v);
+                        t += dot2(g[n], v);
+                    }
+                    d[k] = t;
+                }
+                float w[4];
+                corner_weights(st[jj].lx, st[jj].ly, w);
+                const bool any = st[jj].mask != 0u;
+                const float lx = st[jj].lx, ly = st[jj].ly;
+                // <g, sampled>, <g, d sampled / d x_im>, <g, d sampled / d y_im>
+                float pa = any ? (w[0] * d[0] + w[1] * d[1] + w[2] * d[2] + w[3] * d[3]) : 0.f;
+                float px = any ? ((1.f - ly) * (d[1] - d[0]) + ly * (d[3] - d[2])) : 0.f;
+                float py = any ? ((1.f - lx) * (d[2] - d[0]) + lx * (d[3] - d[1])) : 0.f;
+#pragma unroll
+                for (int o = 1; o < kC; o <<= 1) {
+                    pa += __shfl_xor_sync(0xffffffffu, pa, o);
+                    px += __shfl_xor_sync(0xffffffffu, px, o);
+                    py += __shfl_xor_sync(0xffffffffu, py, o);
+                }
+                if (ln.c == j0 + jj) {
+                    ra = pa;
+                    rx = px;
+                    ry = py;
+                }
+            }
+        }
+        if (live) {
+            const long long ps = (long long)ln.u * a.LK + s_own;
+            ga[ps] = Elem<T>::from_f(ra);
+            gl[2 * ps] = Elem<T>::from_f(wa * lev.fW * rx);
+            gl[2 * ps + 1] = Elem<T>::from_f(wa * lev.fH * ry);
+        }
+
+        // scatter: A * w_corner * g into the inside corners
+        if (!waited) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            waited = true;
+        }
+#pragma unroll
+        for (int j = 0; j < kC; ++j) {
+            const int src = team_lane(ln, j, ln.p);
+            const SampleSetup st = shfl_setup(me, src);
+            const float aj = __shfl_sync(0xffffffffu, wa, src);
+            float w[4];
+            corner_weights(st.lx, st.ly, w);
+            const int off[4] = {st.o, st.o + MD, st.o + st.wmd, st.o + st.wmd + MD};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (!((st.mask >> k) & 1u)) continue;
+                const float2 cf = make_float2(aj * w[k], aj * w[k]);
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    float t[EPV];
+#pragma unroll
+                    for (int e = 0; e < EPV; e += 2) {
+                        const float2 r = __fmul2_rn(cf, make_float2(g[n][e], g[n][e + 1]));
+                        t[e] = r.x;
+                        t[e + 1] = r.y;
+                    }
+                    Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // zero / convert helpers of the backward
 
 // grad_value[i] = round(ws[i]) for i < n (8 elements per step when aligned)

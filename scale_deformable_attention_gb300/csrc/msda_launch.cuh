@@ -17,6 +17,8 @@ struct Plan {
     int nv;        // vectors per lane, 1..4
     bool vec;      // 16-byte slots (else one element per slot)
     bool wide;     // 64-bit offsets inside a batch slice
+    bool spec;     // specialised kernels: C = 4, nvec == 4 * nv, nv <= 3, 32-bit offsets
+    bool pdl;      // backward launched as a programmatic dependent of the zero kernel
 };
 
 #define MSDA_DISPATCH_NV(NVV, ...)                                   \
@@ -37,9 +39,46 @@ static void bwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     msda_bwd_kernel<T, ACC, NV, EPV, WIDE, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
 }
 
+#define MSDA_DISPATCH_NV3(NVV, ...)                                  \
+    switch (NVV) {                                                   \
+    case 1: { constexpr int NV = 1; __VA_ARGS__; } break;            \
+    case 2: { constexpr int NV = 2; __VA_ARGS__; } break;            \
+    default: { constexpr int NV = 3; __VA_ARGS__; } break;           \
+    }
+
+template <typename T, int NV>
+static void fwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    msda_fwd4_kernel<T, NV><<<pl.grid, pl.block, pl.smem, st>>>(a);
+}
+
+template <typename T, typename ACC, int NV>
+static void bwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    if (pl.pdl) {
+        // may start while the zero kernel that precedes it still runs; the
+        // kernel waits (griddepcontrol.wait) before its first scatter
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = pl.grid;
+        cfg.blockDim = pl.block;
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, msda_bwd4_kernel<T, ACC, NV>, a);
+    } else {
+        msda_bwd4_kernel<T, ACC, NV><<<pl.grid, pl.block, pl.smem, st>>>(a);
+    }
+}
+
 template <typename T>
 void launch_forward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     constexpr int VE = 16 / sizeof(T);
+    if (pl.spec) {
+        MSDA_DISPATCH_NV3(pl.nv, (fwd4_go<T, NV>(a, pl, st)))
+        return;
+    }
     if (pl.vec) {
         if (pl.wide) { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, true>(a, pl, st))) }
         else { MSDA_DISPATCH_NV(pl.nv, (fwd_go<T, NV, VE, false>(a, pl, st))) }
@@ -52,6 +91,10 @@ void launch_forward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
 template <typename T, typename ACC>
 void launch_backward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     constexpr int VE = 16 / sizeof(T);
+    if (pl.spec) {
+        MSDA_DISPATCH_NV3(pl.nv, (bwd4_go<T, ACC, NV>(a, pl, st)))
+        return;
+    }
     if (pl.vec) {
         if (pl.wide) { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, true>(a, pl, st))) }
         else { MSDA_DISPATCH_NV(pl.nv, (bwd_go<T, ACC, NV, VE, false>(a, pl, st))) }
