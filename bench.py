@@ -294,7 +294,10 @@ def run_ours(args):
     device = torch.device("cuda", local)
     import scale_deformable_attention_gb300 as msda
 
-    wl = rank_workload(W.WORKLOADS[args.workload], rank)
+    wl = W.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.with_(B=args.batch)
+    wl = rank_workload(wl, rank)
     inp = W.make_inputs(wl)
     accum = args.accum or wl.accum
     st = GpuStep(wl, inp, accum, device)
@@ -514,6 +517,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decoder_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size B")
     ap.add_argument("--accum", choices=["auto", "native", "fp32"], default=None,
                     help="grad_value accumulator (default: the workload's)")
     ap.add_argument("--all", action="store_true", help="also print per-workload fwd/bwd tables")

@@ -2,6 +2,8 @@
 // launch planning and kernel launches on the caller's stream.  No call here
 // synchronises, allocates device memory or reads device memory, except
 // msda_device_errors() and msda_trace_read(), which are documented to wait.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -47,6 +49,7 @@ bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) %
 struct DeviceInfo {
     bool init = false;
     int sms = 0;
+    int l2_bytes = 0;
     unsigned* err = nullptr;  // device address of g_msda_err on this device
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -69,6 +72,8 @@ msda_status device_info(DeviceInfo** out) {
     DeviceInfo& d = g_dev[dev];
     if (!d.init) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_msda_err);
@@ -123,6 +128,8 @@ struct TraceScope {
 struct Tune {
     int C = 0, P = 0, params = -1;
     bool generic = false;  // force the generic kernels
+    bool notma = false;    // no TMA-gather forward
+    bool tma = false;      // TMA-gather forward whatever the size
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -138,6 +145,8 @@ const Tune& tune() {
             else if (!strcmp(tok, "params=ld")) r.params = msda::PARAMS_SMEM_LD;
             else if (!strcmp(tok, "params=direct")) r.params = msda::PARAMS_DIRECT;
             else if (!strcmp(tok, "generic")) r.generic = true;
+            else if (!strcmp(tok, "notma")) r.notma = true;
+            else if (!strcmp(tok, "tma")) r.tma = true;
         }
         return r;
     }();
@@ -232,11 +241,11 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
         NV = (nvec + C - 1) / C;
     }
     // point lanes: enough lanes to fill the GPU, within one warp (C*P <= 32)
-    // and L*K.  Measured on GB300: the forward wants ~768 lanes per SM (one
-    // resident wave at its register count), the backward at least two point
-    // lanes per unit and ~384 lanes per SM.
+    // and L*K.  Measured on GB300: ~768 lanes per SM (one resident wave at
+    // these register counts) for both kernels, and at least two point lanes
+    // per unit for the backward.
     int P = 1;
-    const int64_t target = (int64_t)sms * (backward ? 384 : 768);
+    const int64_t target = (int64_t)sms * 768;
     while (P * C < 32 && P * 2 <= LK && d.units * C * P < target) P *= 2;
     if (backward && P == 1 && C < 32 && LK >= 2) P = 2;
     if (t.P > 0 && (t.P & (t.P - 1)) == 0 && t.P * C <= 32) P = t.P;
@@ -282,6 +291,40 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && NV <= 3 && !t.generic;
     pl.pdl = false;
     return MSDA_OK;
+}
+
+// ---- tensor map of value for the TMA-gather forward ----
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encode_tiled() {
+    static EncodeTiled fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiled) nullptr;
+        return (EncodeTiled)p;
+    }();
+    return fn;
+}
+
+// value as a 2-D tensor of `rows` rows of D elements; one-row boxes of D
+// elements (the gather4 box); coordinates outside read zeros.
+bool value_tensor_map(msda_dtype dt, const void* value, int64_t rows, int64_t D, CUtensorMap* map) {
+    EncodeTiled f = encode_tiled();
+    if (!f) return false;
+    const CUtensorMapDataType t = dt == MSDA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : dt == MSDA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(D * (int64_t)esize(dt))};
+    const cuuint32_t box[2] = {(cuuint32_t)D, 1u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return f(map, t, 2, const_cast<void*>(value), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int grid_for(int64_t n, int sms) {
@@ -394,11 +437,34 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
     a.out = out;
     a.err = di->err;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // TMA-gather forward: whole 16-byte rows, L*K in {4, 8, 16, 32}, row
+    // coordinates of the [B*S*M, D] view below 2^31, and a value tensor
+    // larger than the L2.  Measured on GB300: with value far above the L2
+    // (gathers served by DRAM) the gathers are faster than 16-byte loads
+    // (stress workload forward -24%); with value inside the L2 the load path
+    // is faster (encoder workload forward +59% with gathers).
+    const int LK = (int)(L * K);
+    const bool big = d.n_value * (int64_t)es > (int64_t)di->l2_bytes;
+    CUtensorMap map;
+    const bool tma = pl.spec && !tune().notma && (big || tune().tma) && (LK == 4 || LK == 8 || LK == 16 || LK == 32) &&
+                     B * S * M < (1ll << 31) && value_tensor_map(dt, value, B * S * M, D, &map);
     TraceScope ts(st);
-    switch (dt) {
-    case MSDA_F32: msda::launch_forward<float>(a, pl, st); break;
-    case MSDA_F16: msda::launch_forward<__half>(a, pl, st); break;
-    default: msda::launch_forward<__nv_bfloat16>(a, pl, st); break;
+    if (tma) {
+        a.lc = 2;
+        a.lp = ilog2(LK / 4);
+        const int64_t groups = (d.units * LK + 31) / 32;
+        const unsigned grid = (unsigned)((groups + msda::kTmaWarps - 1) / msda::kTmaWarps);
+        switch (dt) {
+        case MSDA_F32: msda::launch_forward_tma<float>(a, map, pl.nv, grid, st); break;
+        case MSDA_F16: msda::launch_forward_tma<__half>(a, map, pl.nv, grid, st); break;
+        default: msda::launch_forward_tma<__nv_bfloat16>(a, map, pl.nv, grid, st); break;
+        }
+    } else {
+        switch (dt) {
+        case MSDA_F32: msda::launch_forward<float>(a, pl, st); break;
+        case MSDA_F16: msda::launch_forward<__half>(a, pl, st); break;
+        default: msda::launch_forward<__nv_bfloat16>(a, pl, st); break;
+        }
     }
     ts.end(MSDA_KERNEL_FORWARD, d.units);
     cudaError_t e = cudaGetLastError();

@@ -34,6 +34,8 @@
 
 #include <type_traits>
 
+#include <cuda.h>  // CUtensorMap
+
 #include "../../include/msda.h"
 
 namespace msda {
@@ -63,7 +65,8 @@ struct Level {
     long long w_md;      // W * M * D (one image row)
     float fH, fW;
     int ok;              // passed the shape check
-    int pad_;
+    int W;               // level width
+    long long start;     // level_start_index
 };
 
 struct KernelArgs {
@@ -331,7 +334,8 @@ __device__ __forceinline__ bool prologue(const KernelArgs& a, Level* lv, unsigne
         v.fH = ok ? (float)H : 0.f;
         v.fW = ok ? (float)W : 0.f;
         v.ok = ok;
-        v.pad_ = 0;
+        v.W = ok ? (int)W : 0;
+        v.start = ok ? st : 0;
         lv[tid] = v;
         if (!ok) atomicOr(a.err, kErrBadLevel);
     }
@@ -964,6 +968,174 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                 }
             }
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Forward with TMA gathers (rows of whole 16-byte vectors, L*K in {4, 8, 16,
+// 32}, B*S*M < 2^31).  `value` is seen as a 2-D tensor of B*S*M rows of D
+// channels; one cp.async.bulk.tensor ... tile::gather4 brings the four
+// corner rows of a sample into shared memory, so a warp keeps 32 samples
+// (32 x 4 rows) in flight without holding registers or L1 miss slots for
+// them.  Each warp takes 32 / (L*K) units: lane t sets up sample t, writes
+// its four coefficients (A * w_corner, 0 outside) to shared memory and
+// issues the gather; a corner outside the level gets row -1, which the
+// copy fills with zeros.  The copies complete on the warp's mbarrier, waited
+// with a bounded number of polls; then the same lanes, as C = 4 channel
+// lanes x P = L*K/4 point lanes per unit, accumulate from shared memory.
+
+constexpr int kTmaWarps = 4;
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2,
+                                            int r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(map), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
+// bytes of dynamic shared memory of msda_fwd_tma_kernel<T, NV>
+template <typename T, int NV>
+constexpr int fwd_tma_smem() {
+    return kTmaWarps * (32 * 4 * kC * NV * 16 + 32 * 16) + 128;
+}
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kTmaWarps * 32) msda_fwd_tma_kernel(const KernelArgs a,
+                                                                      const __grid_constant__ CUtensorMap tmap) {
+    constexpr int EPV = 16 / sizeof(T);
+    constexpr int ROWB = kC * NV * 16;  // bytes of one D-row
+    constexpr int SAMPLEB = 4 * ROWB;   // four corner rows
+    constexpr int STAGEB = 32 * SAMPLEB;
+    using S_ = Slot<T, EPV>;
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ __align__(8) uint64_t wbar[kTmaWarps];
+    extern __shared__ unsigned char sm_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 127) & ~(uintptr_t)127);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x < a.L) {
+        const int l = threadIdx.x;
+        const long long H = a.shapes[2 * l], W = a.shapes[2 * l + 1], st = a.starts[l];
+        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
+                        H * W <= a.S - st;
+        const long long MD = (long long)a.M * a.D;
+        Level v;
+        v.start_md = ok ? st * MD : 0;
+        v.w_md = ok ? W * MD : 0;
+        v.fH = ok ? (float)H : 0.f;
+        v.fW = ok ? (float)W : 0.f;
+        v.ok = ok;
+        v.W = ok ? (int)W : 0;
+        v.start = ok ? st : 0;
+        lv[l] = v;
+        if (!ok) atomicOr(a.err, kErrBadLevel);
+    }
+    const uint32_t bar = smem_u32(&wbar[warp]);
+    if (lane == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int lgLK = a.lp + 2;  // L*K = 4P lanes per unit
+    const int LK = 1 << lgLK;
+    const int G = 32 >> lgLK;   // units per warp
+    const uint32_t n_groups = ((uint32_t)a.n_units + G - 1) / G;
+    const uint32_t grp = blockIdx.x * (uint32_t)kTmaWarps + warp;
+    if (grp >= n_groups) return;  // the whole warp leaves together
+
+    unsigned char* stage = sm + warp * STAGEB;
+    float4* coef = reinterpret_cast<float4*>(sm + kTmaWarps * STAGEB) + warp * 32;
+
+    // ---- setup: lane = (unit ul, sample s)
+    const int ul = lane >> lgLK;
+    const int s = lane & (LK - 1);
+    const uint32_t u = grp * G + ul;
+    const bool live = u < (uint32_t)a.n_units;
+    const uint32_t b = live ? fdiv(u, a.div_qm) : 0u;
+    const uint32_t m = live ? u - fdiv(u, a.div_m) * (uint32_t)a.M : 0u;
+    float x = -4.f, y = -4.f, w = 0.f;
+    int l = 0;
+    if (live) {
+        const long long ps = (long long)u * LK + s;
+        const T* pl = reinterpret_cast<const T*>(a.loc) + 2 * ps;
+        x = ldg_f(pl);
+        y = ldg_f(pl + 1);
+        w = ldg_f(reinterpret_cast<const T*>(a.attn) + ps);
+        l = (int)fdiv((uint32_t)s, a.div_k);
+    }
+    Level lev = lv[l];
+    if (!live) lev.ok = 0;
+    const float xi = __fmaf_rn(x, lev.fW, -0.5f);
+    const float yi = __fmaf_rn(y, lev.fH, -0.5f);
+    const float x0f = floorf(xi), y0f = floorf(yi);
+    const bool vx0 = lev.ok && x0f >= 0.f && x0f < lev.fW;
+    const bool vx1 = lev.ok && x0f >= -1.f && x0f < lev.fW - 1.f;
+    const bool vy0 = y0f >= 0.f && y0f < lev.fH;
+    const bool vy1 = y0f >= -1.f && y0f < lev.fH - 1.f;
+    const int x0 = (vx0 || vx1) ? (int)x0f : 0;
+    const int y0 = (vy0 || vy1) ? (int)y0f : 0;
+    // row of corner (y0, x0) in the [B*S*M, D] view: (b*S + pixel)*M + m
+    const int row0 = (int)(((long long)b * a.S + lev.start + (long long)y0 * lev.W + x0) * a.M + m);
+    const int wm = lev.W * a.M;
+    const bool ok[4] = {vy0 && vx0, vy0 && vx1, vy1 && vx0, vy1 && vx1};
+    float wk[4];
+    corner_weights(xi - x0f, yi - y0f, wk);
+    coef[lane] = make_float4(ok[0] ? w * wk[0] : 0.f, ok[1] ? w * wk[1] : 0.f, ok[2] ? w * wk[2] : 0.f,
+                             ok[3] ? w * wk[3] : 0.f);
+    const unsigned issuing = __ballot_sync(0xffffffffu, live);
+    if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                     "r"((uint32_t)(__popc(issuing) * SAMPLEB))
+                     : "memory");
+    __syncwarp();
+    if (live)
+        tma_gather4(smem_u32(stage + lane * SAMPLEB), &tmap, 0, ok[0] ? row0 : -1, ok[1] ? row0 + a.M : -1,
+                    ok[2] ? row0 + wm : -1, ok[3] ? row0 + wm + a.M : -1, bar);
+
+    uint32_t done = 0;
+    for (int it = 0; it < (1 << 22) && !done; ++it) done = mbar_try_wait(bar, 0);
+    if (!__all_sync(0xffffffffu, done)) {
+        if (lane == 0) atomicOr(a.err, kErrBulkTimeout);
+        for (int it = 0; it < (1 << 22) && !done; ++it) done = mbar_try_wait(bar, 0);
+        return;
+    }
+
+    // ---- accumulate: lane = (unit ul, channel lane c, point lane p)
+    const int c = s & (kC - 1), p = s >> 2, P = LK >> 2;
+    float acc[NV][EPV];
+#pragma unroll
+    for (int n = 0; n < NV; ++n)
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[n][e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int slot = (ul << lgLK) + p + i * P;
+        const float4 cf4 = coef[slot];
+        const float cf[4] = {cf4.x, cf4.y, cf4.z, cf4.w};
+        const unsigned char* base = stage + slot * SAMPLEB + c * 16;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int n = 0; n < NV; ++n) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(base + k * ROWB + n * kC * 16);
+                float v[EPV];
+                S_::unpack(raw, v);
+                axpy2(acc[n], cf[k], v);
+            }
+    }
+    for (int o = kC; o < LK; o <<= 1) {
+#pragma unroll
+        for (int n = 0; n < NV; ++n)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[n][e] += __shfl_xor_sync(0xffffffffu, acc[n][e], o);
+    }
+    if (live && p == 0) {
+        T* o = reinterpret_cast<T*>(a.out) + (long long)u * a.D + c * EPV;
+#pragma unroll
+        for (int n = 0; n < NV; ++n) S_::store(o + n * kC * EPV, acc[n]);
     }
 }
 

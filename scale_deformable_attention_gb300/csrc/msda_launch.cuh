@@ -104,6 +104,19 @@ void launch_backward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     }
 }
 
+template <typename T, int NV>
+static void fwd_tma_go(const KernelArgs& a, const CUtensorMap& map, unsigned grid, cudaStream_t st) {
+    constexpr int smem = fwd_tma_smem<T, NV>();
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(msda_fwd_tma_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    msda_fwd_tma_kernel<T, NV><<<grid, kTmaWarps * 32, smem, st>>>(a, map);
+}
+
+template <typename T>
+void launch_forward_tma(const KernelArgs& a, const CUtensorMap& map, int nv, unsigned grid, cudaStream_t st) {
+    MSDA_DISPATCH_NV3(nv, (fwd_tma_go<T, NV>(a, map, grid, st)))
+}
+
 template <typename T>
 void launch_convert(const float* ws, T* gv, long long n, int vec, int grid, cudaStream_t st) {
     msda_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, vec);
@@ -118,6 +131,7 @@ void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st
 // defined in msda_kernels_<dtype>.cu
 #define MSDA_EXTERN_IO(T)                                                                  \
     extern template void launch_forward<T>(const KernelArgs&, const Plan&, cudaStream_t); \
+    extern template void launch_forward_tma<T>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t); \
     extern template void launch_backward<T, float>(const KernelArgs&, const Plan&, cudaStream_t);
 MSDA_EXTERN_IO(float)
 MSDA_EXTERN_IO(__half)

@@ -1,0 +1,23 @@
+"""Every kernel family against the oracle, whatever the size heuristics pick:
+the TMA-gather forward, the generic kernels, direct (unstaged) parameter
+loads, and the staged loads without the bulk copy.  Each runs in a child
+process with MSDA_TUNE set."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8"])
+def test_kernel_family(tune):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, MSDA_TUNE=tune)
+    r = subprocess.run([sys.executable, os.path.join(HERE, "path_parity_main.py")], env=env, capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]

@@ -129,6 +129,22 @@ def test_levels_points(L, K):
     assert_grad("f32", f64(ga), rga, "grad_attn")
 
 
+@pytest.mark.parametrize("dtype,D,K", [("bf16", 32, 1), ("bf16", 32, 2), ("bf16", 32, 8), ("f16", 64, 2),
+                                       ("f32", 48, 1), ("f32", 32, 8), ("bf16", 96, 4)])
+def test_forward_widths_and_point_counts(dtype, D, K):
+    """Whole 16-byte rows with L*K in {4, 8, 16, 32} (the TMA-gather forward)
+    and ragged unit counts."""
+    wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, D=D, K=K, B=2, Q=37, M=3,
+                                           shapes=((11, 13), (6, 7), (3, 5), (2, 2)))
+    inp = W.make_inputs(wl)
+    out, gv, gl, ga = _run(wl, inp, "native" if dtype != "f32" else "auto")
+    assert_forward(dtype, f64(out), oracle.forward(inp, dtype), f"D={D} K={K}")
+    rgv, rgl, rga = oracle.backward(inp, dtype)
+    assert_grad(dtype, f64(gv), rgv, "grad_value")
+    assert_grad(dtype, f64(gl), rgl, "grad_loc")
+    assert_grad(dtype, f64(ga), rga, "grad_attn")
+
+
 def test_misaligned_pointers_take_elementwise_path():
     """value / grad_out starting 2 bytes past a 16-byte boundary: same results."""
     msda = _msda()
