@@ -130,6 +130,7 @@ struct Tune {
     bool generic = false;  // force the generic kernels
     bool notma = false;    // no TMA-gather forward
     bool tma = false;      // TMA-gather forward whatever the size
+    bool pointparallel = false;  // the point-parallel ablation forward (D = 32 only)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -147,6 +148,7 @@ const Tune& tune() {
             else if (!strcmp(tok, "generic")) r.generic = true;
             else if (!strcmp(tok, "notma")) r.notma = true;
             else if (!strcmp(tok, "tma")) r.tma = true;
+            else if (!strcmp(tok, "pointparallel")) r.pointparallel = true;
         }
         return r;
     }();
@@ -449,7 +451,15 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
     const bool tma = pl.spec && !tune().notma && (big || tune().tma) && (LK == 4 || LK == 8 || LK == 16 || LK == 32) &&
                      B * S * M < (1ll << 31) && value_tensor_map(dt, value, B * S * M, D, &map);
     TraceScope ts(st);
-    if (tma) {
+    if (tune().pointparallel && D == msda::kPpD && msda::kBlockThreads % LK == 0 && !pl.wide) {
+        const int upb = msda::kBlockThreads / LK;
+        const unsigned grid = (unsigned)((d.units + upb - 1) / upb);
+        switch (dt) {
+        case MSDA_F32: msda::launch_forward_pointparallel<float>(a, grid, st); break;
+        case MSDA_F16: msda::launch_forward_pointparallel<__half>(a, grid, st); break;
+        default: msda::launch_forward_pointparallel<__nv_bfloat16>(a, grid, st); break;
+        }
+    } else if (tma) {
         a.lc = 2;
         a.lp = ilog2(LK / 4);
         const int64_t groups = (d.units * LK + 31) / 32;

@@ -1140,6 +1140,82 @@ __global__ void __launch_bounds__(kTmaWarps * 32) msda_fwd_tma_kernel(const Kern
 }
 
 // ---------------------------------------------------------------------------
+// Point-parallel forward (ablation only, selected with MSDA_TUNE=pointparallel):
+// the decomposition the course calls the obvious port (ch. 4, "The design
+// question"): one thread per sampling point (b, q, m, l, k) reads its four
+// corners channel by channel on its own and keeps a D-float partial sum; the
+// L*K threads of a unit then combine their partials through shared memory.
+// Threads of a warp read unrelated rows, so each scalar load uses a few
+// bytes of its sector.  Kept to compare occupancy and bandwidth with the
+// team decomposition above; D = 32, L*K dividing 256.
+
+constexpr int kPpD = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_fwd_pointparallel_kernel(const KernelArgs a) {
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ float part[kBlockThreads][kPpD + 1];
+    if (threadIdx.x < a.L) {
+        const int l = threadIdx.x;
+        const long long H = a.shapes[2 * l], W = a.shapes[2 * l + 1], st = a.starts[l];
+        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
+                        H * W <= a.S - st;
+        const long long MD = (long long)a.M * a.D;
+        Level v;
+        v.start_md = ok ? st * MD : 0;
+        v.w_md = ok ? W * MD : 0;
+        v.fH = ok ? (float)H : 0.f;
+        v.fW = ok ? (float)W : 0.f;
+        v.ok = ok;
+        v.W = ok ? (int)W : 0;
+        v.start = ok ? st : 0;
+        lv[l] = v;
+        if (!ok) atomicOr(a.err, kErrBadLevel);
+    }
+    __syncthreads();
+    const int LK = a.LK;
+    const int upb = kBlockThreads / LK;  // units per block
+    const int t = threadIdx.x;
+    const uint32_t u = blockIdx.x * (uint32_t)upb + t / LK;
+    const int s = t % LK;
+    const bool live = t < upb * LK && u < (uint32_t)a.n_units;
+    float acc[kPpD];
+#pragma unroll
+    for (int d = 0; d < kPpD; ++d) acc[d] = 0.f;
+    if (live) {
+        const uint32_t b = fdiv(u, a.div_qm);
+        const uint32_t m = u - fdiv(u, a.div_m) * (uint32_t)a.M;
+        const T* vbase = reinterpret_cast<const T*>(a.value) + (long long)b * a.slice + (long long)m * a.D;
+        const long long ps = (long long)u * LK + s;
+        const float x = ldg_f(reinterpret_cast<const T*>(a.loc) + 2 * ps);
+        const float y = ldg_f(reinterpret_cast<const T*>(a.loc) + 2 * ps + 1);
+        const float w = ldg_f(reinterpret_cast<const T*>(a.attn) + ps);
+        const Level lev = lv[fdiv((uint32_t)s, a.div_k)];
+        Corners<int> cr;
+        bilinear_setup<int>(lev, x, y, a.M * a.D, cr);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (!cr.ok[k]) continue;
+            const float c = w * cr.w[k];
+#pragma unroll
+            for (int d = 0; d < kPpD; ++d) acc[d] = fmaf(c, ldg_f(vbase + cr.off[k] + d), acc[d]);
+        }
+    }
+#pragma unroll
+    for (int d = 0; d < kPpD; ++d) part[t][d] = acc[d];
+    __syncthreads();
+    // combine: thread t sums channel t % 32 of unit t / 32 over its L*K partials
+    for (int i = t; i < upb * kPpD; i += kBlockThreads) {
+        const int ul = i / kPpD, d = i % kPpD;
+        const uint32_t uu = blockIdx.x * (uint32_t)upb + ul;
+        if (uu >= (uint32_t)a.n_units) continue;
+        float sum = 0.f;
+        for (int j = 0; j < LK; ++j) sum += part[ul * LK + j][d];
+        reinterpret_cast<T*>(a.out)[(long long)uu * a.D + d] = Elem<T>::from_f(sum);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // zero / convert helpers of the backward
 
 // grad_value[i] = round(ws[i]) for i < n (8 elements per step when aligned)

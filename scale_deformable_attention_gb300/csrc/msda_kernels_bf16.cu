@@ -5,6 +5,7 @@
 namespace msda {
 template void launch_forward<__nv_bfloat16>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_forward_tma<__nv_bfloat16>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t);
+template void launch_forward_pointparallel<__nv_bfloat16>(const KernelArgs&, unsigned, cudaStream_t);
 template void launch_backward<__nv_bfloat16, __nv_bfloat16>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_backward<__nv_bfloat16, float>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_convert<__nv_bfloat16>(const float*, __nv_bfloat16*, long long, int, int, cudaStream_t);

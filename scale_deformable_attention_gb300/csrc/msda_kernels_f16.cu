@@ -5,6 +5,7 @@
 namespace msda {
 template void launch_forward<__half>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_forward_tma<__half>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t);
+template void launch_forward_pointparallel<__half>(const KernelArgs&, unsigned, cudaStream_t);
 template void launch_backward<__half, __half>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_backward<__half, float>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_convert<__half>(const float*, __half*, long long, int, int, cudaStream_t);

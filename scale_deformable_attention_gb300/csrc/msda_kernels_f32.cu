@@ -5,5 +5,6 @@
 namespace msda {
 template void launch_forward<float>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_forward_tma<float>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t);
+template void launch_forward_pointparallel<float>(const KernelArgs&, unsigned, cudaStream_t);
 template void launch_backward<float, float>(const KernelArgs&, const Plan&, cudaStream_t);
 }  // namespace msda

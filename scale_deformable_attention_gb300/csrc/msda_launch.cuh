@@ -118,6 +118,11 @@ void launch_forward_tma(const KernelArgs& a, const CUtensorMap& map, int nv, uns
 }
 
 template <typename T>
+void launch_forward_pointparallel(const KernelArgs& a, unsigned grid, cudaStream_t st) {
+    msda_fwd_pointparallel_kernel<T><<<grid, kBlockThreads, 0, st>>>(a);
+}
+
+template <typename T>
 void launch_convert(const float* ws, T* gv, long long n, int vec, int grid, cudaStream_t st) {
     msda_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, vec);
 }
@@ -132,6 +137,7 @@ void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st
 #define MSDA_EXTERN_IO(T)                                                                  \
     extern template void launch_forward<T>(const KernelArgs&, const Plan&, cudaStream_t); \
     extern template void launch_forward_tma<T>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t); \
+    extern template void launch_forward_pointparallel<T>(const KernelArgs&, unsigned, cudaStream_t); \
     extern template void launch_backward<T, float>(const KernelArgs&, const Plan&, cudaStream_t);
 MSDA_EXTERN_IO(float)
 MSDA_EXTERN_IO(__half)

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8"])
+@pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
