@@ -443,7 +443,7 @@ def run_workload_table(name: str, args, device):
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
     out = {}
-    accums = ["native", "fp32"] if wl.dtype != "f32" else ["auto"]
+    accums = ["native", "fp32", "deterministic"] if wl.dtype != "f32" else ["auto", "deterministic"]
     corners = inbounds_corners(wl, inp)
     model = byte_model(wl, corners)
     peak, _ = peaks()
@@ -518,7 +518,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decoder_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size B")
-    ap.add_argument("--accum", choices=["auto", "native", "fp32"], default=None,
+    ap.add_argument("--accum", choices=["auto", "native", "fp32", "deterministic"], default=None,
                     help="grad_value accumulator (default: the workload's)")
     ap.add_argument("--all", action="store_true", help="also print per-workload fwd/bwd tables")
     ap.add_argument("--no-e2e", action="store_true")

@@ -75,8 +75,23 @@ typedef enum { MSDA_F32 = 0, MSDA_F16 = 1, MSDA_BF16 = 2 } msda_dtype;
  * FP32:   relaxed fp32 vector atomic adds into a caller-provided fp32
  *         workspace, then one rounding pass into grad_value.
  * AUTO:   the choice msda_resolve_accum() returns.
- * For MSDA_F32 all three are the same path (fp32 atomics, no workspace). */
-typedef enum { MSDA_ACCUM_AUTO = 0, MSDA_ACCUM_NATIVE = 1, MSDA_ACCUM_FP32 = 2 } msda_accum;
+ * For MSDA_F32, AUTO / NATIVE / FP32 are the same path (fp32 atomics, no
+ * workspace).
+ * DETERMINISTIC (any dtype): grad_value bit-identical from run to run (the
+ * pages' atomics make it order-dependent; course ch. 5, "Atomics make
+ * gradients nondeterministic").  Each contribution A*w*g, computed in fp32,
+ * is scaled by 2^F and rounded once to a 64-bit integer; the integers are
+ * summed with relaxed 64-bit integer atomic adds, which are exact and
+ * therefore independent of order, then scaled back and rounded once to the
+ * dtype.  F = 61 - ceil(log2(Q*L*K * max|A| * max|g|)) is chosen on the
+ * device per call, so no sum can overflow.  Workspace: 256 + B*S*M*D*8
+ * bytes. */
+typedef enum {
+    MSDA_ACCUM_AUTO = 0,
+    MSDA_ACCUM_NATIVE = 1,
+    MSDA_ACCUM_FP32 = 2,
+    MSDA_ACCUM_DETERMINISTIC = 3
+} msda_accum;
 
 typedef enum {
     MSDA_OK = 0,
@@ -114,12 +129,14 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
                          const void* attention_weights, void* out, msda_stream_t stream);
 
 /* Workspace bytes msda_backward needs for (dt, mode) and the value size:
- * B*S*M*D*4 when the resolved accumulator is FP32 for fp16/bf16, else 0. */
+ * B*S*M*D*4 when the resolved accumulator is FP32 for fp16/bf16,
+ * 256 + B*S*M*D*8 for DETERMINISTIC, else 0. */
 size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
                                     int64_t L, int64_t K, int64_t Q);
 
 /* The accumulator AUTO resolves to for this problem (NATIVE or FP32; a
- * NATIVE or FP32 request is returned unchanged; MSDA_F32 returns NATIVE). */
+ * NATIVE, FP32 or DETERMINISTIC request is returned unchanged, except that
+ * MSDA_F32 returns NATIVE for AUTO / NATIVE / FP32). */
 msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
                               int64_t L, int64_t K, int64_t Q);
 
@@ -141,8 +158,8 @@ msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t
  * runs (course ch. 5, "Atomics make gradients nondeterministic").
  *
  * `workspace` (device, 16-byte aligned, >= msda_backward_workspace_size()
- * bytes) is used only by the FP32 accumulator and may be NULL otherwise; its
- * contents on entry are irrelevant and are clobbered.
+ * bytes) is used only by the FP32 and DETERMINISTIC accumulators and may be
+ * NULL otherwise; its contents on entry are irrelevant and are clobbered.
  * B == 0, Q == 0, M == 0 or D == 0: only the zeroing of grad_value runs.
  * Requirements as msda_forward.
  */

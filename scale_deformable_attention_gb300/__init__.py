@@ -125,7 +125,8 @@ def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_inde
              ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """(grad_value, grad_sampling_locations, grad_attention_weights) (C ABI ``msda_backward``).
 
-    ``accum``: "auto" | "native" | "fp32" accumulator of grad_value for fp16 / bf16.
+    ``accum``: "auto" | "native" | "fp32" accumulator of grad_value for fp16 / bf16, or
+    "deterministic" (any dtype: run-to-run bit-identical grad_value).
     ``accumulate``: add into the given ``grad_value`` instead of overwriting it.
     """
     value, ss, lsi, loc, attn, dims = _prepare(value, spatial_shapes, level_start_index, sampling_locations,
@@ -146,7 +147,7 @@ def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_inde
     grad_attn = torch.empty_like(attn)
     need = workspace_size(value.dtype, accum, dims)
     if need and workspace is None:
-        workspace = torch.empty(need // 4, dtype=torch.float32, device=value.device)
+        workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=value.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     flags = BWD_ACCUMULATE if accumulate else 0
     with torch.cuda.device(value.device):

@@ -16,7 +16,7 @@ LIB_PATH = os.environ.get("MSDA_LIBRARY") or os.path.join(PKG, "libmsda.so")
 MSDA_OK = 0
 STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTED", 3: "MSDA_ERR_MISALIGNED",
                 4: "MSDA_ERR_WORKSPACE", 5: "MSDA_ERR_CUDA"}
-ACCUM = {"auto": 0, "native": 1, "fp32": 2}
+ACCUM = {"auto": 0, "native": 1, "fp32": 2, "deterministic": 3}
 ACCUM_NAMES = {v: k for k, v in ACCUM.items()}
 BWD_ACCUMULATE = 1
 KERNEL_NAMES = {0: "forward", 1: "backward", 2: "zero", 3: "convert"}

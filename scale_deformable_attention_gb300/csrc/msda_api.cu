@@ -280,6 +280,8 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     a.nvec = nvec;
     a.tpb = tpb;
     a.param_mode = mode;
+    a.Q = (int)d.Q;
+    a.det = nullptr;
 
     pl.block = dim3(msda::kBlockThreads);
     const int64_t blocks = (d.units + tpb - 1) / tpb;
@@ -377,6 +379,103 @@ msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
 namespace msda {
 msda_status set_error(msda_status s, const char* message) { return fail(s, "%s", message); }
 }  // namespace msda
+
+namespace {
+
+// Deterministic accumulator: zero the workspace (header + int64 sums), take
+// max |g| and max |A| into the header, run the backward into the int64 sums
+// (launched as a programmatic dependent of the maxima kernel: its gather
+// phase overlaps; the scale is read after griddepcontrol.wait), then convert.
+msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d, const void* value,
+                                   const int64_t* shapes, const int64_t* starts, const void* loc, const void* attn,
+                                   const void* grad_out, void* grad_value, void* grad_loc, void* grad_attn,
+                                   void* workspace, size_t workspace_bytes, cudaStream_t st) {
+    const size_t need = (size_t)d.n_value * 8 + (size_t)msda::kDetHeaderBytes;
+    if (!workspace || workspace_bytes < need)
+        return fail(MSDA_ERR_WORKSPACE, "the deterministic accumulator needs a %zu-byte workspace (got %zu at %p)",
+                    need, workspace_bytes, workspace);
+    if (!aligned(workspace, 16)) return fail(MSDA_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+    DeviceInfo* di = nullptr;
+    msda_status s = device_info(&di);
+    if (s) return s;
+    const size_t es = esize(dt);
+    msda::DetHeader* hdr = static_cast<msda::DetHeader*>(workspace);
+    long long* sums = reinterpret_cast<long long*>(static_cast<unsigned char*>(workspace) + msda::kDetHeaderBytes);
+    if ((s = launch_zero(workspace, (int64_t)need, di->sms, st))) return s;
+    {
+        TraceScope ts(st);
+        const int64_t ng = d.units * d.D, na = d.n_param;
+        const int grid = grid_for((ng > na ? ng : na) / 8 + 1, di->sms);
+        switch (dt) {
+        case MSDA_F32:
+            msda::launch_det_max<float>(static_cast<const float*>(grad_out), ng, static_cast<const float*>(attn), na,
+                                        hdr, grid, st);
+            break;
+        case MSDA_F16:
+            msda::launch_det_max<__half>(static_cast<const __half*>(grad_out), ng, static_cast<const __half*>(attn), na,
+                                         hdr, grid, st);
+            break;
+        default:
+            msda::launch_det_max<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(grad_out), ng,
+                                                static_cast<const __nv_bfloat16*>(attn), na, hdr, grid, st);
+            break;
+        }
+        ts.end(MSDA_KERNEL_CONVERT, ng + na);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "maxima kernel launch");
+    }
+    const bool vec = (d.D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16);
+    KernelArgs a{};
+    Plan pl{};
+    if ((s = make_plan(dt, d, vec, di->sms, true, loc, attn, pl, a))) return s;
+    a.value = value;
+    a.shapes = shapes;
+    a.starts = starts;
+    a.loc = loc;
+    a.attn = attn;
+    a.grad_out = grad_out;
+    a.grad_acc = sums;
+    a.grad_loc = grad_loc;
+    a.grad_attn = grad_attn;
+    a.err = di->err;
+    a.det = hdr;
+    pl.pdl = pl.spec && !trace_active();
+    {
+        TraceScope ts(st);
+        switch (dt) {
+        case MSDA_F32: msda::launch_backward<float, long long>(a, pl, st); break;
+        case MSDA_F16: msda::launch_backward<__half, long long>(a, pl, st); break;
+        default: msda::launch_backward<__nv_bfloat16, long long>(a, pl, st); break;
+        }
+        ts.end(MSDA_KERNEL_BACKWARD, d.units);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
+    }
+    {
+        TraceScope ts(st);
+        const int grid = grid_for(d.n_value, di->sms);
+        const long long qlk = d.Q * d.L * d.K;
+        const int acc = accumulate ? 1 : 0;
+        switch (dt) {
+        case MSDA_F32:
+            msda::launch_det_convert<float>(sums, static_cast<float*>(grad_value), d.n_value, hdr, qlk, acc, grid, st);
+            break;
+        case MSDA_F16:
+            msda::launch_det_convert<__half>(sums, static_cast<__half*>(grad_value), d.n_value, hdr, qlk, acc, grid, st);
+            break;
+        default:
+            msda::launch_det_convert<__nv_bfloat16>(sums, static_cast<__nv_bfloat16*>(grad_value), d.n_value, hdr, qlk,
+                                                    acc, grid, st);
+            break;
+        }
+        ts.end(MSDA_KERNEL_CONVERT, d.n_value);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
+    }
+    return MSDA_OK;
+}
+
+}  // namespace
 
 // ---------------------------------------------------------------------------
 // C ABI
@@ -484,6 +583,7 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
 msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L,
                               int64_t K, int64_t Q) {
     (void)B, (void)M, (void)D;
+    if (mode == MSDA_ACCUM_DETERMINISTIC) return mode;
     if (dt == MSDA_F32) return MSDA_ACCUM_NATIVE;
     if (mode == MSDA_ACCUM_NATIVE || mode == MSDA_ACCUM_FP32) return mode;
     // AUTO: native 16-bit reductions unless many samples land on each pixel,
@@ -495,8 +595,13 @@ msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t
 
 size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
                                     int64_t L, int64_t K, int64_t Q) {
-    if (dt != MSDA_F16 && dt != MSDA_BF16) return 0;
     if (B < 0 || S < 0 || M < 0 || D < 0) return 0;
+    if (mode == MSDA_ACCUM_DETERMINISTIC) {
+        int64_t n;
+        if (!mul_ok(B, S, &n) || !mul_ok(n, M, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 8, &n)) return SIZE_MAX;
+        return (size_t)(n + msda::kDetHeaderBytes);
+    }
+    if (dt != MSDA_F16 && dt != MSDA_BF16) return 0;
     if (msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q) != MSDA_ACCUM_FP32) return 0;
     int64_t n;
     if (!mul_ok(B, S, &n) || !mul_ok(n, M, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 4, &n)) return SIZE_MAX;
@@ -513,7 +618,8 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
     Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
     msda_status s = check_dims(dt, d);
     if (s != MSDA_OK) return s;
-    if (mode != MSDA_ACCUM_AUTO && mode != MSDA_ACCUM_NATIVE && mode != MSDA_ACCUM_FP32)
+    if (mode != MSDA_ACCUM_AUTO && mode != MSDA_ACCUM_NATIVE && mode != MSDA_ACCUM_FP32 &&
+        mode != MSDA_ACCUM_DETERMINISTIC)
         return fail(MSDA_ERR_INVALID_ARG, "unknown accumulator mode %d", (int)mode);
     if (flags & ~MSDA_BWD_ACCUMULATE) return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     const bool accumulate = (flags & MSDA_BWD_ACCUMULATE) != 0;
@@ -532,6 +638,11 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
             return s;
     }
     const msda_accum acc = msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q);
+    if (acc == MSDA_ACCUM_DETERMINISTIC && work && d.n_value > 0)
+        return backward_deterministic(dt, accumulate, d, value, spatial_shapes, level_start_index, sampling_locations,
+                                      attention_weights, grad_out, grad_value, grad_sampling_locations,
+                                      grad_attention_weights, workspace, workspace_bytes,
+                                      reinterpret_cast<cudaStream_t>(stream));
     const bool use_ws = dt != MSDA_F32 && acc == MSDA_ACCUM_FP32 && work && d.n_value > 0;
     if (use_ws) {
         const size_t need = (size_t)d.n_value * 4;

@@ -90,7 +90,51 @@ struct KernelArgs {
     int nvec;              // vectors per D-row
     int tpb;               // units (teams) per block
     int param_mode;        // ParamMode
+    int Q;                 // queries
+    const struct DetHeader* det;  // deterministic accumulator: maxima for the fixed-point scale
 };
+
+// Head of the deterministic accumulator's workspace (256 bytes, then the
+// int64 sums): bit patterns of max |A| and max |g| (non-negative floats
+// order like their bits, so atomicMax on the bits is an order-free max).
+struct DetHeader {
+    unsigned max_attn_bits;
+    unsigned max_g_bits;
+    unsigned pad[62];
+};
+constexpr long long kDetHeaderBytes = 256;
+
+// 2^F with F = 61 - e, where Q*L*K * max|A| * max|g| = f * 2^e, f in [0.5, 1):
+// no element of grad_value takes more than Q*L*K contributions, each of
+// magnitude <= max|A| * max|g| (bilinear weights are <= 1), so after scaling
+// every partial sum stays below 2^61 (plus Q*L*K/2 of rounding), one bit of
+// margin for the float rounding of the bound.  A zero bound gives F = 61; a
+// non-finite one F = 0.
+__device__ __forceinline__ float det_scale(const DetHeader* h, long long qlk) {
+    const float bound = (float)qlk * __uint_as_float(h->max_attn_bits) * __uint_as_float(h->max_g_bits);
+    int F = 61;
+    if (bound > 0.f && bound <= 3.0e38f) {
+        int e = 0;
+        frexpf(bound, &e);
+        F = 61 - e;
+    } else if (!(bound == 0.f)) {
+        F = 0;
+    }
+    F = max(-120, min(120, F));
+    return ldexpf(1.f, F);
+}
+
+__device__ __forceinline__ void red_s64(long long* p, long long v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"((unsigned long long)v) : "memory");
+}
+
+// Deterministic scatter: each fp32 contribution times 2^F (exact) rounded once
+// to an integer, summed with integer atomics (exact, so order-free).
+template <int EPV>
+__device__ __forceinline__ void det_scatter(long long* p, const float (&c)[EPV], float scale) {
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) red_s64(p + e, __float2ll_rn(c[e] * scale));
+}
 
 // ---------------------------------------------------------------------------
 // element types
@@ -560,6 +604,8 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
 
     T* gl = reinterpret_cast<T*>(a.grad_loc);
     T* ga = reinterpret_cast<T*>(a.grad_attn);
+    float dscale = 0.f;
+    if constexpr (std::is_same<ACC, long long>::value) dscale = det_scale(a.det, (long long)a.Q * a.LK);
 
     for (int s0 = 0; s0 < a.LK; s0 += ln.P * U) {
         typename S_::Raw vals[U][4][NV];
@@ -637,7 +683,10 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd_kernel(const KernelArg
                         float t[EPV];
 #pragma unroll
                         for (int e = 0; e < EPV; ++e) t[e] = cf * g[n][e];
-                        Scatter<ACC, EPV>::add(gbase + cr[i].off[k] + j * EPV, t);
+                        if constexpr (std::is_same<ACC, long long>::value)
+                            det_scatter<EPV>(gbase + cr[i].off[k] + j * EPV, t, dscale);
+                        else
+                            Scatter<ACC, EPV>::add(gbase + cr[i].off[k] + j * EPV, t);
                     }
                 }
             }
@@ -865,6 +914,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
     T* gl = reinterpret_cast<T*>(a.grad_loc);
     T* ga = reinterpret_cast<T*>(a.grad_attn);
     bool waited = false;
+    float dscale = 0.f;  // deterministic accumulator: 2^F, read after the wait
 
     for (int r0 = 0; r0 < a.LK; r0 += ln.TP) {
         const int s_own = r0 + ln.p + ln.c * ln.P;
@@ -942,6 +992,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
         if (!waited) {
             asm volatile("griddepcontrol.wait;" ::: "memory");
             waited = true;
+            if constexpr (std::is_same<ACC, long long>::value) dscale = det_scale(a.det, (long long)a.Q * a.LK);
         }
 #pragma unroll
         for (int j = 0; j < kC; ++j) {
@@ -964,7 +1015,10 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                         t[e] = r.x;
                         t[e + 1] = r.y;
                     }
-                    Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                    if constexpr (std::is_same<ACC, long long>::value)
+                        det_scatter<EPV>(gbase + off[k] + n * kC * EPV, t, dscale);
+                    else
+                        Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
                 }
             }
         }
@@ -1212,6 +1266,65 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd_pointparallel_kernel(c
         float sum = 0.f;
         for (int j = 0; j < LK; ++j) sum += part[ul * LK + j][d];
         reinterpret_cast<T*>(a.out)[(long long)uu * a.D + d] = Elem<T>::from_f(sum);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// deterministic accumulator: maxima and conversion
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// max |g| and max |A| into the header (order-free: atomicMax on the bits of
+// non-negative floats; NaN compares false and is skipped)
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_det_max_kernel(const T* g, long long ng, const T* attn,
+                                                                     long long na, DetHeader* h) {
+    // the backward (a programmatic dependent) may start its gather phase now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    __shared__ float red[2][kBlockThreads / 32];
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    float mg = 0.f, ma = 0.f;
+    for (long long i = tid; i < ng; i += nth) mg = fmaxf(mg, fabsf(Elem<T>::to_f(g[i])));
+    for (long long i = tid; i < na; i += nth) ma = fmaxf(ma, fabsf(Elem<T>::to_f(attn[i])));
+    mg = warp_max(mg);
+    ma = warp_max(ma);
+    if ((threadIdx.x & 31) == 0) {
+        red[0][threadIdx.x >> 5] = mg;
+        red[1][threadIdx.x >> 5] = ma;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        mg = threadIdx.x < kBlockThreads / 32 ? red[0][threadIdx.x] : 0.f;
+        ma = threadIdx.x < kBlockThreads / 32 ? red[1][threadIdx.x] : 0.f;
+        mg = warp_max(mg);
+        ma = warp_max(ma);
+        if (threadIdx.x == 0) {
+            atomicMax(&h->max_g_bits, __float_as_uint(mg));
+            atomicMax(&h->max_attn_bits, __float_as_uint(ma));
+        }
+    }
+}
+
+// grad_value[i] = dtype(sum[i] * 2^-F (+ grad_value[i] when accumulating)),
+// the integer converted to double and scaled exactly, then one rounding.
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_det_convert_kernel(const long long* ws, T* gv, long long n,
+                                                                         const DetHeader* h, long long qlk,
+                                                                         int accumulate) {
+    const double inv = 1.0 / (double)det_scale(h, qlk);
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    for (long long i = tid; i < n; i += nth) {
+        double v = __ll2double_rn(ws[i]) * inv;
+        if (accumulate) v += (double)Elem<T>::to_f(gv[i]);
+        if constexpr (sizeof(T) == 4) gv[i] = __double2float_rn(v);
+        else if constexpr (std::is_same<T, __half>::value) gv[i] = __double2half(v);
+        else gv[i] = __double2bfloat16(v);
     }
 }
 

@@ -10,4 +10,8 @@ template void launch_backward<__half, __half>(const KernelArgs&, const Plan&, cu
 template void launch_backward<__half, float>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_convert<__half>(const float*, __half*, long long, int, int, cudaStream_t);
 template void launch_widen<__half>(const __half*, float*, long long, int, cudaStream_t);
+template void launch_backward<__half, long long>(const KernelArgs&, const Plan&, cudaStream_t);
+template void launch_det_max<__half>(const __half*, long long, const __half*, long long, DetHeader*, int, cudaStream_t);
+template void launch_det_convert<__half>(const long long*, __half*, long long, const DetHeader*, long long, int, int,
+                                      cudaStream_t);
 }  // namespace msda

@@ -123,6 +123,17 @@ void launch_forward_pointparallel(const KernelArgs& a, unsigned grid, cudaStream
 }
 
 template <typename T>
+void launch_det_max(const T* g, long long ng, const T* attn, long long na, DetHeader* h, int grid, cudaStream_t st) {
+    msda_det_max_kernel<T><<<grid, kBlockThreads, 0, st>>>(g, ng, attn, na, h);
+}
+
+template <typename T>
+void launch_det_convert(const long long* ws, T* gv, long long n, const DetHeader* h, long long qlk, int accumulate,
+                        int grid, cudaStream_t st) {
+    msda_det_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, h, qlk, accumulate);
+}
+
+template <typename T>
 void launch_convert(const float* ws, T* gv, long long n, int vec, int grid, cudaStream_t st) {
     msda_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, vec);
 }
@@ -138,7 +149,11 @@ void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st
     extern template void launch_forward<T>(const KernelArgs&, const Plan&, cudaStream_t); \
     extern template void launch_forward_tma<T>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t); \
     extern template void launch_forward_pointparallel<T>(const KernelArgs&, unsigned, cudaStream_t); \
-    extern template void launch_backward<T, float>(const KernelArgs&, const Plan&, cudaStream_t);
+    extern template void launch_backward<T, float>(const KernelArgs&, const Plan&, cudaStream_t);             \
+    extern template void launch_backward<T, long long>(const KernelArgs&, const Plan&, cudaStream_t);         \
+    extern template void launch_det_max<T>(const T*, long long, const T*, long long, DetHeader*, int, cudaStream_t); \
+    extern template void launch_det_convert<T>(const long long*, T*, long long, const DetHeader*, long long, int, int, \
+                                               cudaStream_t);
 MSDA_EXTERN_IO(float)
 MSDA_EXTERN_IO(__half)
 MSDA_EXTERN_IO(__nv_bfloat16)

@@ -120,6 +120,12 @@ def test_backward_rejects_mode_and_flags(lib):
     assert bwd(lib, flags=4) == 1 and "flags" in msg(lib)
 
 
+def test_backward_deterministic_needs_workspace(lib):
+    assert bwd(lib, dt=F32, mode=3) == 4 and "deterministic" in msg(lib)
+    n = GOOD["B"] * GOOD["S"] * GOOD["M"] * GOOD["D"]
+    assert bwd(lib, dt=BF16, mode=3, ws=FAKE, ws_bytes=256 + 8 * n - 1) == 4
+
+
 def test_backward_null_grad_value(lib):
     p = [FAKE] * 9
     p[6] = None
@@ -149,6 +155,10 @@ def test_workspace_size_and_resolution(lib):
     assert lib.msda_resolve_accum(BF16, 1, *dims) == 1
     assert lib.msda_resolve_accum(BF16, 2, *dims) == 2
     assert lib.msda_resolve_accum(F16, 0, *dims) in (1, 2)
+    # deterministic accumulator: any dtype, 256-byte header + int64 sums
+    for dt in (F32, F16, BF16):
+        assert lib.msda_backward_workspace_size(dt, 3, *dims) == 256 + 8 * n
+        assert lib.msda_resolve_accum(dt, 3, *dims) == 3
     # many samples per pixel: bf16 AUTO goes to the fp32 accumulator
     dense = (2, 22223, 8, 32, 4, 4, 22223)
     assert lib.msda_resolve_accum(BF16, 0, *dense) == 2
