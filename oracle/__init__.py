@@ -106,7 +106,7 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _prob(inp: Dict[str, np.ndarray], dtype: str, coord_mode: int):
+def _prob(inp: Dict[str, np.ndarray], dtype: str, coord_mode: int, param_dtype: str = ""):
     value = np.ascontiguousarray(inp["value"])
     shapes = np.ascontiguousarray(inp["spatial_shapes"], dtype=np.int64)
     starts = np.ascontiguousarray(inp["level_start_index"], dtype=np.int64)
@@ -117,7 +117,8 @@ def _prob(inp: Dict[str, np.ndarray], dtype: str, coord_mode: int):
     Q, K = loc.shape[1], loc.shape[4]
     dims = (B, S, M, D, L, K, Q)
     keep = (value, shapes, starts, loc, attn)
-    args = [_DT[dtype], int(coord_mode), *dims, _ptr(value), _ptr(shapes), _ptr(starts), _ptr(loc), _ptr(attn)]
+    code = _DT[dtype] | ((_DT[param_dtype] + 1) << 8 if param_dtype else 0)
+    args = [code, int(coord_mode), *dims, _ptr(value), _ptr(shapes), _ptr(starts), _ptr(loc), _ptr(attn)]
     return dims, args, keep
 
 
@@ -126,9 +127,9 @@ def _check(rc: int, what: str):
         raise ValueError(f"oracle {what}: invalid problem (code {rc})")
 
 
-def forward(inp, dtype: str, coord_mode: int = 1, nthreads: int = 0) -> np.ndarray:
-    """out [B, Q, M*D] in fp64."""
-    (B, S, M, D, L, K, Q), args, keep = _prob(inp, dtype, coord_mode)
+def forward(inp, dtype: str, coord_mode: int = 1, nthreads: int = 0, param_dtype: str = "") -> np.ndarray:
+    """out [B, Q, M*D] in fp64 (param_dtype: storage of loc / attn when it differs from value's)."""
+    (B, S, M, D, L, K, Q), args, keep = _prob(inp, dtype, coord_mode, param_dtype)
     out = np.zeros((B, Q, M * D), dtype=np.float64)
     _check(_lib().msda_oracle_forward(*args, _ptr(out), nthreads), "forward")
     return out
@@ -143,10 +144,10 @@ def forward_units(inp, dtype: str, units: np.ndarray, coord_mode: int = 1, nthre
     return out
 
 
-def backward(inp, dtype: str, coord_mode: int = 1, nthreads: int = 0
+def backward(inp, dtype: str, coord_mode: int = 1, nthreads: int = 0, param_dtype: str = ""
              ) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """(grad_value [B,S,M,D], grad_loc [B,Q,M,L,K,2], grad_attn [B,Q,M,L,K]) in fp64."""
-    (B, S, M, D, L, K, Q), args, keep = _prob(inp, dtype, coord_mode)
+    (B, S, M, D, L, K, Q), args, keep = _prob(inp, dtype, coord_mode, param_dtype)
     gout = np.ascontiguousarray(inp["grad_out"])
     gv = np.zeros((B, S, M, D), dtype=np.float64)
     gl = np.zeros((B, Q, M, L, K, 2), dtype=np.float64)
@@ -176,6 +177,65 @@ def grad_value_rows(inp, dtype: str, rows: np.ndarray, coord_mode: int = 1, nthr
     _check(_lib().msda_oracle_grad_value_rows(*args, _ptr(gout), _ptr(rows), rows.size, _ptr(out), nthreads),
            "grad_value_rows")
     return out
+
+
+# ---------------------------------------------------------------------------
+# fused operator: softmax of the attention logits and the sampling locations
+# from reference points and pixel offsets, around the same core
+#
+# msda-triton README, "The operator": A is softmax-normalised over the L*K
+# (level, point) pairs of a query and head; the location is the reference
+# point mapped to level l plus the learned offset.  Reading taken: offsets are
+# in pixels of level l, so loc = ref + offset / (W_l, H_l) (x by W, y by H).
+
+def fused_core_inputs(inp, dtype: str, coord_mode: int = 1):
+    """(core inputs with fp64 loc / attn, A [B,Q,M,L,K], normaliser [L,2]) of a
+    fused problem.  coord_mode 1 computes loc = ref + off / W in binary32 (one
+    rounding per operation, as the kernel does) so the cell decision matches;
+    coord_mode 0 in fp64.  A is the fp64 softmax."""
+    from workloads import to_f64
+
+    ref = to_f64(inp["reference_points"], dtype)        # [B,Q,L,2]
+    off = to_f64(inp["sampling_offsets"], dtype)        # [B,Q,M,L,K,2]
+    logits = to_f64(inp["attention_logits"], dtype)     # [B,Q,M,L*K]
+    shapes = np.asarray(inp["spatial_shapes"], dtype=np.int64)
+    B, Q, M, L, K, _ = off.shape
+    norm = np.stack([shapes[:, 1], shapes[:, 0]], axis=-1).astype(np.float64)   # [L,2] = (W, H)
+    refb = ref[:, :, None, :, None, :]
+    nb = norm[None, None, None, :, None, :]
+    if coord_mode == 1:
+        loc = (refb.astype(np.float32) + off.astype(np.float32) / nb.astype(np.float32)).astype(np.float64)
+    else:
+        loc = refb + off / nb
+    z = logits - logits.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    A = (e / e.sum(axis=-1, keepdims=True)).reshape(B, Q, M, L, K)
+    core = {"value": inp["value"], "spatial_shapes": shapes, "level_start_index": inp["level_start_index"],
+            "sampling_locations": np.ascontiguousarray(loc), "attention_weights": np.ascontiguousarray(A)}
+    if "grad_out" in inp:
+        core["grad_out"] = inp["grad_out"]
+    return core, A, norm
+
+
+def fused_forward(inp, dtype: str, coord_mode: int = 1, nthreads: int = 0) -> np.ndarray:
+    core, _, _ = fused_core_inputs(inp, dtype, coord_mode)
+    return forward(core, dtype, coord_mode, nthreads, param_dtype="f64")
+
+
+def fused_backward(inp, dtype: str, coord_mode: int = 1, nthreads: int = 0):
+    """(grad_value, grad_reference_points [B,Q,L,2], grad_sampling_offsets [B,Q,M,L,K,2],
+    grad_attention_logits [B,Q,M,L*K]) by the chain rule through the core:
+    d loc / d offset = 1 / (W_l, H_l), d loc / d ref = 1 (summed over heads and
+    points), and the softmax backward A * (gA - <A, gA>)."""
+    core, A, norm = fused_core_inputs(inp, dtype, coord_mode)
+    gv, gl, ga = backward(core, dtype, coord_mode, nthreads, param_dtype="f64")
+    B, Q, M, L, K, _ = gl.shape
+    g_off = gl / norm[None, None, None, :, None, :]
+    g_ref = gl.sum(axis=(2, 4))
+    A2 = A.reshape(B, Q, M, L * K)
+    ga2 = ga.reshape(B, Q, M, L * K)
+    g_logit = A2 * (ga2 - (A2 * ga2).sum(axis=-1, keepdims=True))
+    return gv, g_ref, g_off, g_logit
 
 
 # ---------------------------------------------------------------------------

@@ -85,13 +85,14 @@ static double load_el(const void* base, int64_t i, int dt) {
 /* ---- the shared problem description ---- */
 
 typedef struct {
-    int dt, coord_mode;
+    int dt, coord_mode;      /* dt: value / grad_out storage */
     int64_t B, S, M, D, L, K, Q;
     const void* value;
     const int64_t* shapes;   /* [L,2] = (H, W) */
     const int64_t* starts;   /* [L] */
     const void* loc;         /* [B,Q,M,L,K,2] */
     const void* attn;        /* [B,Q,M,L,K] */
+    int pdt;                 /* storage of loc / attn (dt unless a caller sets it) */
 } prob_t;
 
 /* One sampling point after the bilinear setup. */
@@ -109,9 +110,9 @@ typedef struct {
 static void setup_sample(const prob_t* P, int64_t b, int64_t q, int64_t m, int64_t l, int64_t k,
                          sample_t* s) {
     int64_t p = (((b * P->Q + q) * P->M + m) * P->L + l) * P->K + k;
-    double x = load_el(P->loc, 2 * p, P->dt);
-    double y = load_el(P->loc, 2 * p + 1, P->dt);
-    s->a = load_el(P->attn, p, P->dt);
+    double x = load_el(P->loc, 2 * p, P->pdt);
+    double y = load_el(P->loc, 2 * p + 1, P->pdt);
+    s->a = load_el(P->attn, p, P->pdt);
     s->H = P->shapes[2 * l];
     s->W = P->shapes[2 * l + 1];
     int64_t start = P->starts[l];
@@ -151,7 +152,7 @@ static inline int64_t value_index(const prob_t* P, int64_t b, int64_t row, int64
 
 static int check_prob(const prob_t* P) {
     if (P->B < 0 || P->S < 0 || P->M < 0 || P->D < 0 || P->L < 0 || P->K < 0 || P->Q < 0) return -1;
-    if (P->dt < 0 || P->dt > 3) return -2;
+    if (P->dt < 0 || P->dt > 3 || P->pdt < 0 || P->pdt > 3) return -2;
     for (int64_t l = 0; l < P->L; ++l) {
         int64_t H = P->shapes[2 * l], W = P->shapes[2 * l + 1], st = P->starts[l];
         if (H < 0 || W < 0 || st < 0 || st + H * W > P->S) return -3;
@@ -182,7 +183,12 @@ static void forward_unit(const prob_t* P, int64_t b, int64_t q, int64_t m, doubl
 #define PROB_ARGS int dt, int coord_mode, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, \
     int64_t K, int64_t Q, const void* value, const int64_t* shapes, const int64_t* starts,      \
     const void* loc, const void* attn
-#define PROB_INIT {dt, coord_mode, B, S, M, D, L, K, Q, value, shapes, starts, loc, attn}
+/* dt: low byte = storage of value / grad_out; a non-zero high byte h gives
+ * loc / attn the storage h - 1 (the fused oracle in oracle/__init__.py passes
+ * the locations and weights it computes as fp64 arrays while value keeps the
+ * I/O dtype); otherwise loc / attn share value's storage. */
+#define PROB_INIT {dt & 0xff, coord_mode, B, S, M, D, L, K, Q, value, shapes, starts, loc, attn, \
+                   (dt >> 8) ? ((dt >> 8) & 0xff) - 1 : (dt & 0xff)}
 
 static void set_threads(int nthreads) {
 #ifdef _OPENMP

@@ -439,8 +439,105 @@ def pin_samplers():
     _close(oracle.grad_value_rows(inp, "bf16", rows), gv.reshape(-1, wl.D)[rows], 1e-13, what="grad_value rows")
 
 
+def _fused_problem(rng, B=2, Q=4, M=2, D=3, K=2, shapes=((4, 6), (3, 5)), spread=2.0):
+    L = len(shapes)
+    S = sum(h * w for h, w in shapes)
+    sh = np.asarray(shapes, dtype=np.int64)
+    return {
+        "value": rng.standard_normal((B, S, M, D)),
+        "spatial_shapes": sh,
+        "level_start_index": W.level_start_index(shapes),
+        "reference_points": rng.uniform(0.1, 0.9, (B, Q, L, 2)),
+        "sampling_offsets": rng.normal(0.0, spread, (B, Q, M, L, K, 2)),
+        "attention_logits": rng.standard_normal((B, Q, M, L * K)),
+        "grad_out": rng.standard_normal((B, Q, M * D)),
+    }
+
+
+def pin_fused_special_cases():
+    """Zero offsets and equal logits: the fused operator is the core with
+    loc = reference point and A = 1/(L*K).  Offsets of (dx*W, dy*H) pixels move
+    the sample by exactly (dx, dy) in normalised coordinates (x by W, y by H;
+    the levels have W != H).  A constant added to a row of logits changes
+    nothing."""
+    rng = np.random.default_rng(31)
+    f = _fused_problem(rng)
+    B, Q, M, L, K = 2, 4, 2, 2, 2
+    f0 = dict(f, sampling_offsets=np.zeros((B, Q, M, L, K, 2)), attention_logits=np.full((B, Q, M, L * K), 0.7))
+    core = _inputs(f["value"], f["spatial_shapes"],
+                   np.broadcast_to(f["reference_points"][:, :, None, :, None, :], (B, Q, M, L, K, 2)),
+                   np.full((B, Q, M, L, K), 1.0 / (L * K)))
+    _close(oracle.fused_forward(f0, "f64", coord_mode=0), oracle.forward(core, "f64", coord_mode=0), 1e-13,
+           what="fused with zero offsets")
+    d = rng.uniform(-0.05, 0.05, (B, Q, M, L, K, 2))
+    wh = np.stack([f["spatial_shapes"][:, 1], f["spatial_shapes"][:, 0]], axis=-1).astype(np.float64)
+    f1 = dict(f0, sampling_offsets=d * wh[None, None, None, :, None, :])
+    core1 = dict(core, sampling_locations=f["reference_points"][:, :, None, :, None, :] + d)
+    _close(oracle.fused_forward(f1, "f64", coord_mode=0), oracle.forward(core1, "f64", coord_mode=0), 1e-12,
+           what="fused offsets normalised by (W, H)")
+    shift = rng.uniform(-3, 3, (B, Q, M, 1))
+    _close(oracle.fused_forward(dict(f, attention_logits=f["attention_logits"] + shift), "f64", coord_mode=0),
+           oracle.fused_forward(f, "f64", coord_mode=0), 1e-12, what="softmax shift invariance")
+    _, _, _, gz = oracle.fused_backward(f, "f64", coord_mode=0)
+    assert np.max(np.abs(gz.sum(-1))) < 1e-12, "logit gradients of a row must sum to zero"
+
+
+def pin_fused_torch_restatement():
+    """The fused operator and its three input gradients equal torch softmax +
+    grid_sample with autograd (fp64, CPU)."""
+    import torch
+
+    rng = np.random.default_rng(32)
+    for _ in range(4):
+        f = _fused_problem(rng)
+        core, _, _ = oracle.fused_core_inputs(f, "f64", coord_mode=0)
+        if _away_from_kinks(core):
+            break
+    t = {k: torch.tensor(v) for k, v in f.items()}
+    for k in ("reference_points", "sampling_offsets", "attention_logits"):
+        t[k].requires_grad_(True)
+    B, Q, M, L, K = 2, 4, 2, 2, 2
+    wh = torch.stack([t["spatial_shapes"][:, 1], t["spatial_shapes"][:, 0]], dim=-1).double()
+    loc = t["reference_points"][:, :, None, :, None, :] + t["sampling_offsets"] / wh[None, None, None, :, None, :]
+    A = torch.softmax(t["attention_logits"], dim=-1).view(B, Q, M, L, K)
+    ref_out = oracle.gridsample_forward(t["value"], f["spatial_shapes"], f["level_start_index"], loc, A)
+    (ref_out * t["grad_out"]).sum().backward()
+    _close(oracle.fused_forward(f, "f64", coord_mode=0), ref_out.detach().numpy(), 1e-12, what="fused out")
+    gv, gr, go, gz = oracle.fused_backward(f, "f64", coord_mode=0)
+    _close(gr, t["reference_points"].grad.numpy(), 1e-11, what="fused grad_reference_points")
+    _close(go, t["sampling_offsets"].grad.numpy(), 1e-11, what="fused grad_sampling_offsets")
+    _close(gz, t["attention_logits"].grad.numpy(), 1e-11, what="fused grad_attention_logits")
+
+
+def pin_fused_finite_differences():
+    """Central differences of <g, out> in fp64 against the fused gradients."""
+    rng = np.random.default_rng(33)
+    for _ in range(20):
+        f = _fused_problem(rng, B=1, Q=2, M=2, D=2, K=2)
+        core, _, _ = oracle.fused_core_inputs(f, "f64", coord_mode=0)
+        if _away_from_kinks(core, tol=1e-3):
+            break
+    else:
+        raise AssertionError("could not draw a kink-free problem")
+    g = f["grad_out"]
+    _, gr, go, gz = oracle.fused_backward(f, "f64", coord_mode=0)
+    h = 1e-6
+    for key, grad in (("reference_points", gr), ("sampling_offsets", go), ("attention_logits", gz)):
+        base = f[key].reshape(-1)
+        fd = np.empty(base.size)
+        for i in range(base.size):
+            p, m = base.copy(), base.copy()
+            p[i] += h
+            m[i] -= h
+            lp = float(np.sum(oracle.fused_forward(dict(f, **{key: p.reshape(f[key].shape)}), "f64", coord_mode=0) * g))
+            lm = float(np.sum(oracle.fused_forward(dict(f, **{key: m.reshape(f[key].shape)}), "f64", coord_mode=0) * g))
+            fd[i] = (lp - lm) / (2 * h)
+        _close(grad.reshape(-1), fd, 1e-6, atol=1e-8, what=f"fused finite differences {key}")
+
+
 ALL_PINS = [
     pin_hand_worked, pin_constant_field, pin_linear_field, pin_pixel_centres, pin_zero_padding,
     pin_convexity, pin_gridsample, pin_brute_force, pin_finite_differences, pin_adjoint,
     pin_scatter_total, pin_fp32_coordinate, pin_coordinate_modes_agree, pin_samplers,
+    pin_fused_special_cases, pin_fused_torch_restatement, pin_fused_finite_differences,
 ]

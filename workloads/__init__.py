@@ -214,12 +214,55 @@ def make_inputs(wl: Workload, *, with_grad: bool = True) -> Dict[str, np.ndarray
     return out
 
 
+def make_fused_inputs(wl: Workload, *, with_grad: bool = True) -> Dict[str, np.ndarray]:
+    """Inputs of the fused operator (reference points, pixel offsets, attention
+    logits) for ``wl``'s sizes and dtype.  Draw order from one PCG64 stream
+    (seed + 100): value, reference points, offsets, logits, grad_out.
+
+    * uniform01 / uniform_wide: reference points ~ U[0,1) / U[-0.1,1.1) per
+      (b, q, l); offsets ~ N(0, 2) pixels of level l.
+    * pixel_centres: the reference point of query q is pyramid pixel q's centre
+      (as the unfused encoder workload); offsets ~ N(0, 0.02 * (W_l, H_l)) pixels.
+    * logits as the workload's attention logits.
+    """
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 100))
+    B, M, D, L, K, S, Q = wl.B, wl.M, wl.D, wl.L, wl.K, wl.S, wl.Qn
+    shapes = np.array(wl.shapes, dtype=np.int64).reshape(L, 2)
+    value = _normal_cast(rng, B * S * M * D, wl.dtype).reshape(B, S, M, D)
+    if wl.loc == "pixel_centres":
+        if Q != S:
+            raise ValueError("pixel_centres needs one query per pyramid pixel (Q == S)")
+        ref = np.broadcast_to(_pixel_centres(wl.shapes)[None, :, None, :], (B, Q, L, 2)).copy()
+        scale = 0.02 * np.stack([shapes[:, 1], shapes[:, 0]], axis=-1)            # [L,2] (W, H)
+        off = rng.standard_normal((B, Q, M, L, K, 2)) * scale[None, None, None, :, None, :]
+    else:
+        lo, hi = (-0.1, 1.1) if wl.loc == "uniform_wide" else (0.0, 1.0)
+        ref = rng.uniform(lo, hi, (B, Q, L, 2))
+        off = rng.normal(0.0, 2.0, (B, Q, M, L, K, 2))
+    if wl.logits == "normal":
+        z = rng.standard_normal((B, Q, M, L * K))
+    else:
+        z = rng.random((B, Q, M, L * K))
+    out = {
+        "value": value,
+        "spatial_shapes": shapes,
+        "level_start_index": level_start_index(wl.shapes),
+        "reference_points": cast(ref, wl.dtype).reshape(B, Q, L, 2),
+        "sampling_offsets": cast(off, wl.dtype).reshape(B, Q, M, L, K, 2),
+        "attention_logits": cast(z, wl.dtype).reshape(B, Q, M, L * K),
+    }
+    if with_grad:
+        out["grad_out"] = _normal_cast(rng, B * Q * M * D, wl.dtype).reshape(B, Q, M * D)
+    return out
+
+
 def scaled(name: str, **kw) -> Workload:
     """A named workload with some sizes overridden (for oracle-sized parity cases)."""
     return WORKLOADS[name].with_(**kw)
 
 
-FLOAT_KEYS = ("value", "sampling_locations", "attention_weights", "grad_out")
+FLOAT_KEYS = ("value", "sampling_locations", "attention_weights", "grad_out", "reference_points",
+              "sampling_offsets", "attention_logits")
 
 
 def to_torch(inp: Dict[str, np.ndarray], dtype: str, device):
