@@ -23,8 +23,8 @@ MUTANTS = [
     ("weight_swap_x", "double wx = j ? s->lx : 1.0 - s->lx;", "double wx = j ? 1.0 - s->lx : s->lx;"),
     ("hw_swap", "s->H = P->shapes[2 * l];\n    s->W = P->shapes[2 * l + 1];",
      "s->W = P->shapes[2 * l];\n    s->H = P->shapes[2 * l + 1];"),
-    ("loc_xy_swap", "double x = load_el(P->loc, 2 * p, P->dt);\n    double y = load_el(P->loc, 2 * p + 1, P->dt);",
-     "double y = load_el(P->loc, 2 * p, P->dt);\n    double x = load_el(P->loc, 2 * p + 1, P->dt);"),
+    ("loc_xy_swap", "double x = load_el(P->loc, 2 * p, P->pdt);\n    double y = load_el(P->loc, 2 * p + 1, P->pdt);",
+     "double y = load_el(P->loc, 2 * p, P->pdt);\n    double x = load_el(P->loc, 2 * p + 1, P->pdt);"),
     ("gloc_drop_attn", "gloc[2 * sl] = s.a * (double)s.W * gx;", "gloc[2 * sl] = (double)s.W * gx;"),
     ("gloc_y_scale", "gloc[2 * sl + 1] = s.a * (double)s.H * gy;", "gloc[2 * sl + 1] = s.a * (double)s.W * gy;"),
     ("dwdx_sign", "s->dwdx[i][j] = wy * (j ? 1.0 : -1.0);", "s->dwdx[i][j] = wy * (j ? -1.0 : 1.0);"),
