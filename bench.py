@@ -369,6 +369,9 @@ def run_ours(args):
     if args.all and rank == 0:
         for name in W.WORKLOADS:
             print(json.dumps(run_workload_table(name, args, device)), flush=True)
+    if args.fused and rank == 0:
+        for name in ("decoder_bf16", "encoder_fp16"):
+            print(json.dumps(run_fused_table(name, args, device)), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -495,6 +498,115 @@ def run_workload_table(name: str, args, device):
     return {"table": name, "units": wl.units, "corners_inside": corners, "bytes_model": model, "results": out}
 
 
+def run_fused_table(name: str, args, device):
+    """Device times of the fused operator (softmax of the logits and
+    loc = ref + offset / (W, H) inside the kernels) against the same operator
+    built from PyTorch ops around the core kernels, on one named workload."""
+    import torch
+
+    import scale_deformable_attention_gb300 as msda
+    from scale_deformable_attention_gb300 import _lib
+
+    wl = W.WORKLOADS[name]
+    inp = W.make_fused_inputs(wl)
+    t = W.to_torch(inp, wl.dtype, device)
+    lib = _lib.lib()
+    dims = (wl.B, wl.S, wl.M, wl.D, wl.L, wl.K, wl.Qn)
+    dt = msda.DTYPE_CODE[t["value"].dtype]
+    B, Q, M, L, K = wl.B, wl.Qn, wl.M, wl.L, wl.K
+    p = lambda x: x.data_ptr()  # noqa: E731
+    out = torch.empty((B, Q, M * wl.D), dtype=t["value"].dtype, device=device)
+    gv = torch.empty_like(t["value"])
+    gr = torch.empty_like(t["reference_points"])
+    go = torch.empty_like(t["sampling_offsets"])
+    gz = torch.empty_like(t["attention_logits"])
+    ss = t["spatial_shapes"]
+    norm = torch.stack([ss[:, 1], ss[:, 0]], -1).to(torch.float32)            # [L, 2] = (W, H)
+    flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    st = lambda: torch.cuda.current_stream(device).cuda_stream  # noqa: E731
+    # pixel coordinates of the fused locations (binary32, as the kernels) for the byte model
+    es = W.ESIZE[wl.dtype]
+    ref = W.to_f64(inp["reference_points"], wl.dtype).astype(np.float32)
+    off = W.to_f64(inp["sampling_offsets"], wl.dtype).astype(np.float32)
+    nrm = np.array([[w, h] for h, w in wl.shapes], dtype=np.float32)
+    loc = ref[:, :, None, :, None, :] + off / nrm[None, None, None, :, None, :]
+    corners = inbounds_corners(wl.with_(dtype="f32"), {"sampling_locations": loc.astype(np.float32)})
+    gather = corners * wl.D * es
+    refb = B * Q * L * 2 * es
+    params = wl.samples * 3 * es
+    rowio = wl.units * wl.D * es
+    n_value = wl.B * wl.S * wl.M * wl.D
+    model = {"forward": gather + refb + params + rowio,
+             "bwd_total": 2 * gather + rowio + refb + 2 * params + n_value * es + wl.samples * 2 * es + refb}
+    res = {}
+    for accum in (["native", "fp32", "deterministic"] if wl.dtype != "f32" else ["auto", "deterministic"]):
+        acc = _lib.ACCUM[accum]
+        need = int(lib.msda_backward_workspace_size(dt, acc, *dims))
+        ws = torch.empty(max(need // 4, 1), dtype=torch.float32, device=device)
+
+        def fwd():
+            _lib.check(lib.msda_forward_fused(dt, *dims, p(t["value"]), p(ss), p(t["level_start_index"]),
+                                              p(t["reference_points"]), p(t["sampling_offsets"]),
+                                              p(t["attention_logits"]), p(out), st()))
+
+        def bwd():
+            _lib.check(lib.msda_backward_fused(dt, acc, 0, *dims, p(t["value"]), p(ss), p(t["level_start_index"]),
+                                               p(t["reference_points"]), p(t["sampling_offsets"]),
+                                               p(t["attention_logits"]), p(t["grad_out"]), p(gv), p(gr), p(go),
+                                               p(gz), p(ws), need, st()))
+
+        # the same operator from PyTorch ops around the core kernels
+        saved = {}
+
+        def fwd_torch():
+            A = torch.softmax(t["attention_logits"].float(), -1).to(t["value"].dtype).view(B, Q, M, L, K)
+            lc = (t["reference_points"].float()[:, :, None, :, None, :] +
+                  t["sampling_offsets"].float() / norm[None, None, None, :, None, :]).to(t["value"].dtype)
+            saved["A"], saved["loc"] = A, lc
+            msda.forward(t["value"], ss, t["level_start_index"], lc, A, out=out, validate=False)
+
+        def bwd_torch():
+            A, lc = saved["A"], saved["loc"]
+            g_v, g_l, g_a = msda.backward(t["value"], ss, t["level_start_index"], lc, A, t["grad_out"], accum=accum,
+                                          grad_value=gv, workspace=ws if need else None, validate=False)
+            g_l = g_l.float()
+            g_off = (g_l / norm[None, None, None, :, None, :]).to(t["value"].dtype)
+            g_ref = g_l.sum(dim=(2, 4)).to(t["value"].dtype)
+            a2 = A.float().reshape(B, Q, M, L * K)
+            ga2 = g_a.float().reshape(B, Q, M, L * K)
+            g_z = (a2 * (ga2 - (a2 * ga2).sum(-1, keepdim=True))).to(t["value"].dtype)
+            return g_v, g_ref, g_off, g_z
+
+        def timed(fn, n):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for a, b in ev:
+                flush_buf.sum()
+                a.record()
+                fn()
+                b.record()
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+        n = 50
+        for _ in range(3):
+            fwd(), bwd(), fwd_torch(), bwd_torch()
+        r = {}
+        for tag, f, b in (("fused", fwd, bwd), ("torch_ops_around_core", fwd_torch, bwd_torch)):
+            tf = timed(f, n)
+            f()
+            tb = timed(b, n)
+            ts = timed(lambda: (f(), b()), n)
+            r[tag] = {"fwd_ms": round(tf, 4), "bwd_ms": round(tb, 4), "step_ms": round(ts, 4)}
+        r["fused"]["fwd_frac_of_measured"] = round(model["forward"] / (r["fused"]["fwd_ms"] / 1e3) / 1e9 / peaks()[0], 4)
+        r["fused"]["bwd_frac_of_measured"] = round(model["bwd_total"] / (r["fused"]["bwd_ms"] / 1e3) / 1e9 /
+                                                   peaks()[0], 4)
+        r["step_speedup"] = round(r["torch_ops_around_core"]["step_ms"] / r["fused"]["step_ms"], 3)
+        res[accum] = r
+        del ws
+    return {"table": "fused", "workload": name, "units": wl.units, "corners_inside": corners, "bytes_model": model,
+            "results": res}
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 
@@ -548,6 +660,8 @@ def main(argv=None):
     ap.add_argument("--accum", choices=["auto", "native", "fp32", "deterministic"], default=None,
                     help="grad_value accumulator (default: the workload's)")
     ap.add_argument("--all", action="store_true", help="also print per-workload fwd/bwd tables")
+    ap.add_argument("--fused", action="store_true",
+                    help="also print fused-operator vs PyTorch-ops-around-the-core tables")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)

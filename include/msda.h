@@ -160,7 +160,8 @@ msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t
  * `workspace` (device, 16-byte aligned, >= msda_backward_workspace_size()
  * bytes) is used only by the FP32 and DETERMINISTIC accumulators and may be
  * NULL otherwise; its contents on entry are irrelevant and are clobbered.
- * B == 0, Q == 0, M == 0 or D == 0: only the zeroing of grad_value runs.
+ * B == 0, Q == 0, M == 0 or D == 0: nothing is sampled and every gradient
+ * is zero (grad_value keeps its contents with MSDA_BWD_ACCUMULATE).
  * Requirements as msda_forward.
  */
 msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M,
@@ -169,6 +170,53 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
                           const void* sampling_locations, const void* attention_weights, const void* grad_out,
                           void* grad_value, void* grad_sampling_locations, void* grad_attention_weights,
                           void* workspace, size_t workspace_bytes, msda_stream_t stream);
+
+/*
+ * Fused operator (msda-triton README, "The operator": the weights A are
+ * softmax-normalised over the L*K (level, point) pairs of a query and head,
+ * and the sampling location is the reference point mapped to level l plus a
+ * learned offset).  The steps on either side of the core are taken inside the
+ * kernels, so sampling_locations and attention_weights never exist in memory:
+ *
+ *   A[b,q,m,l,k]   = softmax over the L*K entries of attention_logits[b,q,m,:]   (fp32)
+ *   loc[b,q,m,l,k] = reference_points[b,q,l] + sampling_offsets[b,q,m,l,k] / (W_l, H_l)
+ *                    (x by W, y by H; offsets are in pixels of level l; fp32, one
+ *                    rounding per operation)
+ *   out            = the core of msda_forward on (loc, A)
+ *
+ * Layouts: reference_points [B, Q, L, 2] (x, y); sampling_offsets
+ * [B, Q, M, L, K, 2]; attention_logits [B, Q, M, L*K]; out [B, Q, M*D].
+ * Needs rows of whole 16-byte vectors (D*esize in {64, 128, 192} bytes:
+ * D = 32/64/96 for bf16/fp16, 16/32/48 for fp32) and 16-byte aligned value /
+ * out / grad pointers; otherwise MSDA_ERR_UNSUPPORTED.  Other requirements
+ * and errors as msda_forward.
+ */
+msda_status msda_forward_fused(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K,
+                               int64_t Q, const void* value, const int64_t* spatial_shapes,
+                               const int64_t* level_start_index, const void* reference_points,
+                               const void* sampling_offsets, const void* attention_logits, void* out,
+                               msda_stream_t stream);
+
+/*
+ * Backward of the fused operator:
+ *
+ *   grad_sampling_offsets[p] = grad_loc[p] / (W_l, H_l)  =  A_p * <g, d sampled_p / d (x_im, y_im)>
+ *   grad_reference_points[b,q,l] = sum over (m, k) of grad_loc[b,q,m,l,k]
+ *   grad_attention_logits[b,q,m,s] = A_s * (gA_s - sum_j A_j gA_j),  gA_s = <g, sampled_s>
+ *   grad_value as msda_backward
+ *
+ * All outputs are overwritten (grad_value accumulates with
+ * MSDA_BWD_ACCUMULATE).  Accumulators, workspace and requirements as
+ * msda_backward and msda_forward_fused.
+ */
+msda_status msda_backward_fused(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M,
+                                int64_t D, int64_t L, int64_t K, int64_t Q, const void* value,
+                                const int64_t* spatial_shapes, const int64_t* level_start_index,
+                                const void* reference_points, const void* sampling_offsets,
+                                const void* attention_logits, const void* grad_out, void* grad_value,
+                                void* grad_reference_points, void* grad_sampling_offsets,
+                                void* grad_attention_logits, void* workspace, size_t workspace_bytes,
+                                msda_stream_t stream);
 
 /*
  * Backward with the FP32 accumulator whose scratch lives in a fixed device

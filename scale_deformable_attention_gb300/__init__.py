@@ -26,7 +26,8 @@ import torch
 from . import _lib
 from ._lib import ACCUM, BWD_ACCUMULATE, MsdaError
 
-__all__ = ["multi_scale_deformable_attention", "forward", "backward", "workspace_size", "resolve_accum",
+__all__ = ["multi_scale_deformable_attention", "multi_scale_deformable_attention_fused", "forward", "backward",
+           "forward_fused", "backward_fused", "workspace_size", "resolve_accum",
            "device_errors", "trace_enable", "trace_pause", "trace_read", "MsdaError", "DTYPE_CODE"]
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -192,6 +193,101 @@ def multi_scale_deformable_attention(value: torch.Tensor, spatial_shapes: torch.
     """
     accum = "auto" if fp32_grad_accum is None else ("fp32" if fp32_grad_accum else "native")
     return _MSDAFunction.apply(value, spatial_shapes, level_start_index, sampling_locations, attention_weights, accum)
+
+
+def _prepare_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets, attention_logits,
+                   validate: bool):
+    if sampling_offsets.dim() != 6 or sampling_offsets.shape[-1] != 2:
+        raise ValueError(f"sampling_offsets must be [B, Q, M, L, K, 2], got {tuple(sampling_offsets.shape)}")
+    B, Q, M, L, K, _ = sampling_offsets.shape
+    if tuple(attention_logits.shape) != (B, Q, M, L * K):
+        raise ValueError(f"attention_logits must be {(B, Q, M, L * K)}, got {tuple(attention_logits.shape)}")
+    if tuple(reference_points.shape) != (B, Q, L, 2):
+        raise ValueError(f"reference_points must be {(B, Q, L, 2)}, got {tuple(reference_points.shape)}")
+    for name, t in (("reference_points", reference_points), ("attention_logits", attention_logits)):
+        if t.dtype != value.dtype or t.device != value.device:
+            raise TypeError(f"{name} must be a {value.dtype} tensor on {value.device}")
+    # the shared checks, with the logits viewed in the weights' layout
+    value, ss, lsi, off, logit5, dims = _prepare(value, spatial_shapes, level_start_index, sampling_offsets,
+                                                 attention_logits.reshape(B, Q, M, L, K), validate)
+    return value, ss, lsi, reference_points.contiguous(), off, logit5.reshape(B, Q, M, L * K), dims
+
+
+def forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets, attention_logits, *,
+                  out=None, validate: bool = True) -> torch.Tensor:
+    """Fused operator (C ABI ``msda_forward_fused``): A = softmax of the logits
+    over L*K, loc = reference point + offset / (W_l, H_l), out[B, Q, M*D]."""
+    value, ss, lsi, ref, off, logit, dims = _prepare_fused(value, spatial_shapes, level_start_index,
+                                                           reference_points, sampling_offsets, attention_logits,
+                                                           validate)
+    B, S, M, D, L, K, Q = dims
+    if out is None:
+        out = torch.empty((B, Q, M * D), dtype=value.dtype, device=value.device)
+    with torch.cuda.device(value.device):
+        _lib.check(_lib.lib().msda_forward_fused(DTYPE_CODE[value.dtype], *dims, _ptr(value), _ptr(ss), _ptr(lsi),
+                                                 _ptr(ref), _ptr(off), _ptr(logit), _ptr(out),
+                                                 _stream(value.device)))
+    return out
+
+
+def backward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets, attention_logits,
+                   grad_out, *, accum: str = "auto", grad_value=None, accumulate: bool = False, workspace=None,
+                   validate: bool = True):
+    """(grad_value, grad_reference_points, grad_sampling_offsets, grad_attention_logits)
+    of the fused operator (C ABI ``msda_backward_fused``)."""
+    value, ss, lsi, ref, off, logit, dims = _prepare_fused(value, spatial_shapes, level_start_index,
+                                                           reference_points, sampling_offsets, attention_logits,
+                                                           validate)
+    B, S, M, D, L, K, Q = dims
+    if grad_out.shape != (B, Q, M * D) or grad_out.dtype != value.dtype:
+        raise ValueError(f"grad_out must be a [B, Q, M*D] {value.dtype} tensor")
+    grad_out = grad_out.contiguous()
+    if grad_value is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs grad_value")
+        grad_value = torch.empty_like(value)
+    g_ref = torch.empty_like(ref)
+    g_off = torch.empty_like(off)
+    g_logit = torch.empty_like(logit)
+    need = workspace_size(value.dtype, accum, dims)
+    if need and workspace is None:
+        workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=value.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(value.device):
+        _lib.check(_lib.lib().msda_backward_fused(
+            DTYPE_CODE[value.dtype], ACCUM[accum], BWD_ACCUMULATE if accumulate else 0, *dims, _ptr(value), _ptr(ss),
+            _ptr(lsi), _ptr(ref), _ptr(off), _ptr(logit), _ptr(grad_out), _ptr(grad_value), _ptr(g_ref),
+            _ptr(g_off), _ptr(g_logit), _ptr(workspace), ws_bytes, _stream(value.device)))
+    return grad_value, g_ref, g_off, g_logit
+
+
+class _MSDAFusedFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                attention_logits, accum):
+        out = forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                            attention_logits)
+        ss = spatial_shapes.to(value.device, torch.int64)
+        lsi = level_start_index_of(ss) if level_start_index is None else level_start_index.to(value.device, torch.int64)
+        ctx.save_for_backward(value, ss, lsi, reference_points, sampling_offsets, attention_logits)
+        ctx.accum = accum
+        return out
+
+    @staticmethod
+    @torch.autograd.function.once_differentiable
+    def backward(ctx, grad_out):
+        value, ss, lsi, ref, off, logit = ctx.saved_tensors
+        gv, gr, go, gz = backward_fused(value, ss, lsi, ref, off, logit, grad_out, accum=ctx.accum, validate=False)
+        return gv, None, None, gr, go, gz, None
+
+
+def multi_scale_deformable_attention_fused(value, spatial_shapes, level_start_index, reference_points,
+                                           sampling_offsets, attention_logits, fp32_grad_accum=None):
+    """Differentiable fused operator: softmax of the logits over L*K and
+    loc = reference point + offset / (W_l, H_l) taken inside the kernels."""
+    accum = "auto" if fp32_grad_accum is None else ("fp32" if fp32_grad_accum else "native")
+    return _MSDAFusedFunction.apply(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
+                                    attention_logits, accum)
 
 
 def device_errors(clear: bool = True) -> int:

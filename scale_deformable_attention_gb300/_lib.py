@@ -45,6 +45,10 @@ def _declare(lib):
     lib.msda_forward.restype = c_int
     lib.msda_backward.argtypes = [c_int, c_int, c_uint] + dims + [vp] * 9 + [vp, sz, vp]
     lib.msda_backward.restype = c_int
+    lib.msda_forward_fused.argtypes = [c_int] + dims + [vp] * 7 + [vp]
+    lib.msda_forward_fused.restype = c_int
+    lib.msda_backward_fused.argtypes = [c_int, c_int, c_uint] + dims + [vp] * 11 + [vp, sz, vp]
+    lib.msda_backward_fused.restype = c_int
     lib.msda_backward_workspace_size.argtypes = [c_int, c_int] + dims
     lib.msda_backward_workspace_size.restype = sz
     lib.msda_resolve_accum.argtypes = [c_int, c_int] + dims

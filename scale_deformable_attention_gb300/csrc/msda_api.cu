@@ -227,7 +227,7 @@ void pick_c(int nvec, int* C, int* NV) {
 }
 
 msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool backward, const void* loc,
-                      const void* attn, Plan& pl, KernelArgs& a) {
+                      const void* attn, Plan& pl, KernelArgs& a, bool fused = false) {
     const int es = (int)esize(dt);
     const int epv = vec ? 16 / es : 1;
     const int nvec = (int)(d.D / epv);
@@ -251,6 +251,10 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     while (P * C < 32 && P * 2 <= LK && d.units * C * P < target) P *= 2;
     if (backward && P == 1 && C < 32 && LK >= 2) P = 2;
     if (t.P > 0 && (t.P & (t.P - 1)) == 0 && t.P * C <= 32) P = t.P;
+    // fused backward: a block keeps <g, sampled> of all its samples in shared
+    // memory (256 / (C*P) units * L*K floats): at most 32 KB
+    if (fused && backward)
+        while ((int64_t)(msda::kBlockThreads / (C * P)) * LK * 4 > 32768 && C * P < 32) P *= 2;
     const int tp = C * P;
     const int tpb = msda::kBlockThreads / tp;
     // parameter staging: one bulk copy when both chunks are 16-byte pieces
@@ -294,7 +298,56 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     pl.vec = vec;
     pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && NV <= 3 && !t.generic;
     pl.pdl = false;
+    pl.fused = fused;
+    a.ref = nullptr;
+    a.gbuf_off = 0;
+    if (fused && backward) {
+        const int64_t gbuf = (int64_t)tpb * LK * 4;
+        int64_t off = mode != msda::PARAMS_DIRECT ? (int64_t)((pl.smem + 15) / 16 * 16) : 0;
+        if (off + gbuf > 48 * 1024) {  // drop the parameter staging
+            a.param_mode = msda::PARAMS_DIRECT;
+            off = 0;
+        }
+        a.gbuf_off = (int)off;
+        pl.smem = (size_t)(off + gbuf);
+    }
+    if (fused && !pl.spec)
+        return fail(MSDA_ERR_UNSUPPORTED,
+                    "the fused operator needs rows of whole 16-byte vectors with 16-byte aligned value / grad "
+                    "pointers and D*esize in {64, 128, 192} bytes (D = %lld)",
+                    (long long)d.D);
     return MSDA_OK;
+}
+
+// Inputs / outputs of the fused operator that the plain one does not have.
+struct Fused {
+    const void* ref;  // reference points [B, Q, L, 2]
+    void* grad_ref;   // their gradient (backward)
+};
+
+msda_status launch_ref_grad(msda_dtype dt, const Dims& d, const int64_t* shapes, const void* grad_off, void* grad_ref,
+                            cudaStream_t st) {
+    const long long BQ = d.B * d.Q;
+    if (BQ * d.L == 0) return MSDA_OK;
+    TraceScope ts(st);
+    switch (dt) {
+    case MSDA_F32:
+        msda::launch_fused_ref_grad<float>(static_cast<const float*>(grad_off), static_cast<float*>(grad_ref), shapes,
+                                           BQ, (int)d.M, (int)d.L, (int)d.K, st);
+        break;
+    case MSDA_F16:
+        msda::launch_fused_ref_grad<__half>(static_cast<const __half*>(grad_off), static_cast<__half*>(grad_ref),
+                                            shapes, BQ, (int)d.M, (int)d.L, (int)d.K, st);
+        break;
+    default:
+        msda::launch_fused_ref_grad<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(grad_off),
+                                                   static_cast<__nv_bfloat16*>(grad_ref), shapes, BQ, (int)d.M,
+                                                   (int)d.L, (int)d.K, st);
+        break;
+    }
+    ts.end(MSDA_KERNEL_CONVERT, BQ * d.L * 2);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "reference-point gradient kernel launch");
 }
 
 // ---- tensor map of value for the TMA-gather forward ----
@@ -389,7 +442,7 @@ namespace {
 msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d, const void* value,
                                    const int64_t* shapes, const int64_t* starts, const void* loc, const void* attn,
                                    const void* grad_out, void* grad_value, void* grad_loc, void* grad_attn,
-                                   void* workspace, size_t workspace_bytes, cudaStream_t st) {
+                                   void* workspace, size_t workspace_bytes, cudaStream_t st, const Fused* fz) {
     const size_t need = (size_t)d.n_value * 8 + (size_t)msda::kDetHeaderBytes;
     if (!workspace || workspace_bytes < need)
         return fail(MSDA_ERR_WORKSPACE, "the deterministic accumulator needs a %zu-byte workspace (got %zu at %p)",
@@ -401,33 +454,36 @@ msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d
     const size_t es = esize(dt);
     msda::DetHeader* hdr = static_cast<msda::DetHeader*>(workspace);
     long long* sums = reinterpret_cast<long long*>(static_cast<unsigned char*>(workspace) + msda::kDetHeaderBytes);
+    // the plan first: a call it rejects enqueues nothing
+    const bool vec = (d.D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16);
+    KernelArgs a{};
+    Plan pl{};
+    if ((s = make_plan(dt, d, vec, di->sms, true, loc, attn, pl, a, fz != nullptr))) return s;
     if ((s = launch_zero(workspace, (int64_t)need, di->sms, st))) return s;
     {
         TraceScope ts(st);
-        const int64_t ng = d.units * d.D, na = d.n_param;
+        // softmax-normalised weights (fused operator) are at most 1: no scan
+        const int64_t ng = d.units * d.D, na = fz ? 0 : d.n_param;
+        const float ma0 = fz ? 1.f : 0.f;
         const int grid = grid_for((ng > na ? ng : na) / 8 + 1, di->sms);
         switch (dt) {
         case MSDA_F32:
             msda::launch_det_max<float>(static_cast<const float*>(grad_out), ng, static_cast<const float*>(attn), na,
-                                        hdr, grid, st);
+                                        ma0, hdr, grid, st);
             break;
         case MSDA_F16:
             msda::launch_det_max<__half>(static_cast<const __half*>(grad_out), ng, static_cast<const __half*>(attn), na,
-                                         hdr, grid, st);
+                                         ma0, hdr, grid, st);
             break;
         default:
             msda::launch_det_max<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(grad_out), ng,
-                                                static_cast<const __nv_bfloat16*>(attn), na, hdr, grid, st);
+                                                static_cast<const __nv_bfloat16*>(attn), na, ma0, hdr, grid, st);
             break;
         }
         ts.end(MSDA_KERNEL_CONVERT, ng + na);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "maxima kernel launch");
     }
-    const bool vec = (d.D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16);
-    KernelArgs a{};
-    Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, true, loc, attn, pl, a))) return s;
     a.value = value;
     a.shapes = shapes;
     a.starts = starts;
@@ -439,6 +495,7 @@ msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d
     a.grad_attn = grad_attn;
     a.err = di->err;
     a.det = hdr;
+    if (fz) a.ref = fz->ref;
     pl.pdl = pl.spec && !trace_active();
     {
         TraceScope ts(st);
@@ -472,6 +529,7 @@ msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
     }
+    if (fz) return launch_ref_grad(dt, d, shapes, grad_loc, fz->grad_ref, st);
     return MSDA_OK;
 }
 
@@ -508,49 +566,45 @@ const char* msda_kernel_name(int k) {
     return "unknown";
 }
 
-msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K, int64_t Q,
-                         const void* value, const int64_t* spatial_shapes, const int64_t* level_start_index,
-                         const void* sampling_locations, const void* attention_weights, void* out,
-                         msda_stream_t stream) {
-    g_msg[0] = 0;
-    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
-    msda_status s = check_dims(dt, d);
-    if (s != MSDA_OK) return s;
-    if (d.units == 0 || D == 0) return MSDA_OK;  // empty output: nothing to launch
+}  // extern "C"
+
+namespace {
+
+// Forward after argument validation; `ref` non-NULL selects the fused operator
+// (loc / attn then hold sampling offsets / attention logits).
+msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const int64_t* spatial_shapes,
+                         const int64_t* level_start_index, const void* loc, const void* attn, void* out,
+                         cudaStream_t st, const void* ref) {
+    msda_status s;
     const size_t es = esize(dt);
-    if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
-        (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
-        (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
-        (s = check_ptr(sampling_locations, true, es, "sampling_locations")) ||
-        (s = check_ptr(attention_weights, true, es, "attention_weights")) || (s = check_ptr(out, true, es, "out")))
-        return s;
     DeviceInfo* di = nullptr;
     if ((s = device_info(&di))) return s;
-    const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(out, 16);
+    const bool vec = (d.D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(out, 16);
     KernelArgs a{};
     Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, false, sampling_locations, attention_weights, pl, a))) return s;
+    if ((s = make_plan(dt, d, vec, di->sms, false, loc, attn, pl, a, ref != nullptr))) return s;
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;
-    a.loc = sampling_locations;
-    a.attn = attention_weights;
+    a.loc = loc;
+    a.attn = attn;
     a.out = out;
     a.err = di->err;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    a.ref = ref;
     // TMA-gather forward: whole 16-byte rows, L*K in {4, 8, 16, 32}, row
     // coordinates of the [B*S*M, D] view below 2^31, and a value tensor
     // larger than the L2.  Measured on GB300: with value far above the L2
     // (gathers served by DRAM) the gathers are faster than 16-byte loads
     // (stress workload forward -24%); with value inside the L2 the load path
     // is faster (encoder workload forward +59% with gathers).
-    const int LK = (int)(L * K);
+    const int LK = (int)(d.L * d.K);
     const bool big = d.n_value * (int64_t)es > (int64_t)di->l2_bytes;
     CUtensorMap map;
-    const bool tma = pl.spec && !tune().notma && (big || tune().tma) && (LK == 4 || LK == 8 || LK == 16 || LK == 32) &&
-                     B * S * M < (1ll << 31) && value_tensor_map(dt, value, B * S * M, D, &map);
+    const bool tma = !ref && pl.spec && !tune().notma && (big || tune().tma) &&
+                     (LK == 4 || LK == 8 || LK == 16 || LK == 32) && d.B * d.S * d.M < (1ll << 31) &&
+                     value_tensor_map(dt, value, d.B * d.S * d.M, d.D, &map);
     TraceScope ts(st);
-    if (tune().pointparallel && D == msda::kPpD && msda::kBlockThreads % LK == 0 && !pl.wide) {
+    if (!ref && tune().pointparallel && d.D == msda::kPpD && msda::kBlockThreads % LK == 0 && !pl.wide) {
         const int upb = msda::kBlockThreads / LK;
         const unsigned grid = (unsigned)((d.units + upb - 1) / upb);
         switch (dt) {
@@ -578,6 +632,52 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
     ts.end(MSDA_KERNEL_FORWARD, d.units);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "forward kernel launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K, int64_t Q,
+                         const void* value, const int64_t* spatial_shapes, const int64_t* level_start_index,
+                         const void* sampling_locations, const void* attention_weights, void* out,
+                         msda_stream_t stream) {
+    g_msg[0] = 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    msda_status s = check_dims(dt, d);
+    if (s != MSDA_OK) return s;
+    if (d.units == 0 || D == 0) return MSDA_OK;  // empty output: nothing to launch
+    const size_t es = esize(dt);
+    if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
+        (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
+        (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
+        (s = check_ptr(sampling_locations, true, es, "sampling_locations")) ||
+        (s = check_ptr(attention_weights, true, es, "attention_weights")) || (s = check_ptr(out, true, es, "out")))
+        return s;
+    return forward_core(dt, d, value, spatial_shapes, level_start_index, sampling_locations, attention_weights, out,
+                        reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+msda_status msda_forward_fused(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K,
+                               int64_t Q, const void* value, const int64_t* spatial_shapes,
+                               const int64_t* level_start_index, const void* reference_points,
+                               const void* sampling_offsets, const void* attention_logits, void* out,
+                               msda_stream_t stream) {
+    g_msg[0] = 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    msda_status s = check_dims(dt, d);
+    if (s != MSDA_OK) return s;
+    if (d.units == 0 || D == 0) return MSDA_OK;
+    const size_t es = esize(dt);
+    if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
+        (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
+        (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
+        (s = check_ptr(reference_points, true, es, "reference_points")) ||
+        (s = check_ptr(sampling_offsets, true, es, "sampling_offsets")) ||
+        (s = check_ptr(attention_logits, true, es, "attention_logits")) || (s = check_ptr(out, true, es, "out")))
+        return s;
+    return forward_core(dt, d, value, spatial_shapes, level_start_index, sampling_offsets, attention_logits, out,
+                        reinterpret_cast<cudaStream_t>(stream), reference_points);
 }
 
 msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L,
@@ -608,41 +708,27 @@ size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, i
     return (size_t)n;
 }
 
-msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M, int64_t D,
-                          int64_t L, int64_t K, int64_t Q, const void* value, const int64_t* spatial_shapes,
-                          const int64_t* level_start_index, const void* sampling_locations,
-                          const void* attention_weights, const void* grad_out, void* grad_value,
-                          void* grad_sampling_locations, void* grad_attention_weights, void* workspace,
-                          size_t workspace_bytes, msda_stream_t stream) {
-    g_msg[0] = 0;
-    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
-    msda_status s = check_dims(dt, d);
-    if (s != MSDA_OK) return s;
-    if (mode != MSDA_ACCUM_AUTO && mode != MSDA_ACCUM_NATIVE && mode != MSDA_ACCUM_FP32 &&
-        mode != MSDA_ACCUM_DETERMINISTIC)
-        return fail(MSDA_ERR_INVALID_ARG, "unknown accumulator mode %d", (int)mode);
-    if (flags & ~MSDA_BWD_ACCUMULATE) return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
-    const bool accumulate = (flags & MSDA_BWD_ACCUMULATE) != 0;
+}  // extern "C"
+
+namespace {
+
+// Backward after argument validation; `fz` non-NULL selects the fused
+// operator (sampling_locations / attention_weights then hold offsets /
+// logits, their gradients go to grad_sampling_locations / grad_attention_weights).
+msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const Dims& d, const void* value,
+                          const int64_t* spatial_shapes, const int64_t* level_start_index,
+                          const void* sampling_locations, const void* attention_weights, const void* grad_out,
+                          void* grad_value, void* grad_sampling_locations, void* grad_attention_weights,
+                          void* workspace, size_t workspace_bytes, cudaStream_t st, const Fused* fz) {
+    const int64_t B = d.B, S = d.S, M = d.M, D = d.D, L = d.L, K = d.K, Q = d.Q;
+    msda_status s;
     const size_t es = esize(dt);
     const bool work = d.units > 0 && D > 0;
-    if ((s = check_ptr(grad_value, d.n_value > 0, es, "grad_value"))) return s;
-    if (work) {
-        if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
-            (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
-            (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
-            (s = check_ptr(sampling_locations, true, es, "sampling_locations")) ||
-            (s = check_ptr(attention_weights, true, es, "attention_weights")) ||
-            (s = check_ptr(grad_out, true, es, "grad_out")) ||
-            (s = check_ptr(grad_sampling_locations, true, es, "grad_sampling_locations")) ||
-            (s = check_ptr(grad_attention_weights, true, es, "grad_attention_weights")))
-            return s;
-    }
     const msda_accum acc = msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q);
     if (acc == MSDA_ACCUM_DETERMINISTIC && work && d.n_value > 0)
         return backward_deterministic(dt, accumulate, d, value, spatial_shapes, level_start_index, sampling_locations,
                                       attention_weights, grad_out, grad_value, grad_sampling_locations,
-                                      grad_attention_weights, workspace, workspace_bytes,
-                                      reinterpret_cast<cudaStream_t>(stream));
+                                      grad_attention_weights, workspace, workspace_bytes, st, fz);
     const bool use_ws = dt != MSDA_F32 && acc == MSDA_ACCUM_FP32 && work && d.n_value > 0;
     if (use_ws) {
         const size_t need = (size_t)d.n_value * 4;
@@ -651,16 +737,32 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
                         workspace_bytes, workspace);
         if (!aligned(workspace, 16)) return fail(MSDA_ERR_WORKSPACE, "workspace is not 16-byte aligned");
     }
-    if (d.n_value == 0 && !work) return MSDA_OK;
+    const bool empty_params = d.n_param == 0 || (fz && d.B * d.Q * d.L == 0);
+    if (d.n_value == 0 && !work && empty_params) return MSDA_OK;
 
     DeviceInfo* di = nullptr;
     if ((s = device_info(&di))) return s;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!work) {
+        // no output channels or no units: every gradient is zero
+        if (!accumulate && (s = launch_zero(grad_value, d.n_value * (int64_t)es, di->sms, st))) return s;
+        if ((s = launch_zero(grad_sampling_locations, d.n_param * 2 * (int64_t)es, di->sms, st))) return s;
+        if ((s = launch_zero(grad_attention_weights, d.n_param * (int64_t)es, di->sms, st))) return s;
+        if (fz && (s = launch_zero(fz->grad_ref, d.B * d.Q * d.L * 2 * (int64_t)es, di->sms, st))) return s;
+        return MSDA_OK;
+    }
+
+    void* acc_buf = use_ws ? workspace : grad_value;
+    const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16) &&
+                     aligned(acc_buf, 16);
+    KernelArgs a{};
+    Plan pl{};
+    // the plan first: a call it rejects enqueues nothing
+    if ((s = make_plan(dt, d, vec, di->sms, true, sampling_locations, attention_weights, pl, a, fz != nullptr)))
+        return s;
 
     // grad_value (or the workspace) must start from zero / from grad_value
     if (!use_ws) {
         if (!accumulate && (s = launch_zero(grad_value, d.n_value * (int64_t)es, di->sms, st))) return s;
-        if (!work) return MSDA_OK;
     } else if (!accumulate) {
         if ((s = launch_zero(workspace, d.n_value * 4, di->sms, st))) return s;
     } else {
@@ -681,12 +783,6 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
     // may be launched as its programmatic dependent (not while tracing, whose
     // events sit between the two launches)
     const bool zeroed_here = !accumulate && (use_ws || d.n_value > 0);
-    void* acc_buf = use_ws ? workspace : grad_value;
-    const bool vec = (D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(grad_out, 16) &&
-                     aligned(acc_buf, 16);
-    KernelArgs a{};
-    Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, true, sampling_locations, attention_weights, pl, a))) return s;
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;
@@ -697,6 +793,7 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
     a.grad_loc = grad_sampling_locations;
     a.grad_attn = grad_attention_weights;
     a.err = di->err;
+    if (fz) a.ref = fz->ref;
     pl.pdl = pl.spec && zeroed_here && !trace_active();
     {
         TraceScope ts(st);
@@ -729,7 +826,87 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
     }
+    if (fz) return launch_ref_grad(dt, d, spatial_shapes, grad_sampling_locations, fz->grad_ref, st);
     return MSDA_OK;
+}
+
+
+// Validation shared by the two backward entry points.
+msda_status backward_checks(msda_dtype dt, msda_accum mode, unsigned flags, Dims& d, const void* value,
+                            const int64_t* spatial_shapes, const int64_t* level_start_index, const void* p_loc,
+                            const char* n_loc, const void* p_attn, const char* n_attn, const void* grad_out,
+                            void* grad_value, void* g_loc, const char* n_gloc, void* g_attn, const char* n_gattn) {
+    msda_status s = check_dims(dt, d);
+    if (s != MSDA_OK) return s;
+    if (mode != MSDA_ACCUM_AUTO && mode != MSDA_ACCUM_NATIVE && mode != MSDA_ACCUM_FP32 &&
+        mode != MSDA_ACCUM_DETERMINISTIC)
+        return fail(MSDA_ERR_INVALID_ARG, "unknown accumulator mode %d", (int)mode);
+    if (flags & ~MSDA_BWD_ACCUMULATE) return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const size_t es = esize(dt);
+    const bool work = d.units > 0 && d.D > 0;
+    if ((s = check_ptr(grad_value, d.n_value > 0, es, "grad_value"))) return s;
+    if ((s = check_ptr(g_loc, d.n_param > 0, es, n_gloc)) || (s = check_ptr(g_attn, d.n_param > 0, es, n_gattn)))
+        return s;
+    if (work) {
+        if ((s = check_ptr(value, d.n_value > 0, es, "value")) ||
+            (s = check_ptr(spatial_shapes, true, 8, "spatial_shapes")) ||
+            (s = check_ptr(level_start_index, true, 8, "level_start_index")) ||
+            (s = check_ptr(p_loc, true, es, n_loc)) || (s = check_ptr(p_attn, true, es, n_attn)) ||
+            (s = check_ptr(grad_out, true, es, "grad_out")))
+            return s;
+    }
+    return MSDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M, int64_t D,
+                          int64_t L, int64_t K, int64_t Q, const void* value, const int64_t* spatial_shapes,
+                          const int64_t* level_start_index, const void* sampling_locations,
+                          const void* attention_weights, const void* grad_out, void* grad_value,
+                          void* grad_sampling_locations, void* grad_attention_weights, void* workspace,
+                          size_t workspace_bytes, msda_stream_t stream) {
+    g_msg[0] = 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    msda_status s = backward_checks(dt, mode, flags, d, value, spatial_shapes, level_start_index, sampling_locations,
+                                    "sampling_locations", attention_weights, "attention_weights", grad_out,
+                                    grad_value, grad_sampling_locations, "grad_sampling_locations",
+                                    grad_attention_weights, "grad_attention_weights");
+    if (s != MSDA_OK) return s;
+    return backward_core(dt, mode, (flags & MSDA_BWD_ACCUMULATE) != 0, d, value, spatial_shapes, level_start_index,
+                         sampling_locations, attention_weights, grad_out, grad_value, grad_sampling_locations,
+                         grad_attention_weights, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                         nullptr);
+}
+
+msda_status msda_backward_fused(msda_dtype dt, msda_accum mode, unsigned flags, int64_t B, int64_t S, int64_t M,
+                                int64_t D, int64_t L, int64_t K, int64_t Q, const void* value,
+                                const int64_t* spatial_shapes, const int64_t* level_start_index,
+                                const void* reference_points, const void* sampling_offsets,
+                                const void* attention_logits, const void* grad_out, void* grad_value,
+                                void* grad_reference_points, void* grad_sampling_offsets,
+                                void* grad_attention_logits, void* workspace, size_t workspace_bytes,
+                                msda_stream_t stream) {
+    g_msg[0] = 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    msda_status s = backward_checks(dt, mode, flags, d, value, spatial_shapes, level_start_index, sampling_offsets,
+                                    "sampling_offsets", attention_logits, "attention_logits", grad_out, grad_value,
+                                    grad_sampling_offsets, "grad_sampling_offsets", grad_attention_logits,
+                                    "grad_attention_logits");
+    if (s != MSDA_OK) return s;
+    const size_t es = esize(dt);
+    const bool nref = d.B * d.Q * d.L > 0;
+    if ((s = check_ptr(grad_reference_points, nref, es, "grad_reference_points")) ||
+        (s = check_ptr(reference_points, nref && d.units > 0 && d.D > 0, es, "reference_points")) ||
+        (s = check_ptr(spatial_shapes, nref, 8, "spatial_shapes")))
+        return s;
+    const Fused fz{reference_points, grad_reference_points};
+    return backward_core(dt, mode, (flags & MSDA_BWD_ACCUMULATE) != 0, d, value, spatial_shapes, level_start_index,
+                         sampling_offsets, attention_logits, grad_out, grad_value, grad_sampling_offsets,
+                         grad_attention_logits, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                         &fz);
 }
 
 msda_status msda_device_errors(uint32_t* bits, int clear) {

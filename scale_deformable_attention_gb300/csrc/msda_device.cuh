@@ -92,6 +92,10 @@ struct KernelArgs {
     int param_mode;        // ParamMode
     int Q;                 // queries
     const struct DetHeader* det;  // deterministic accumulator: maxima for the fixed-point scale
+    // fused operator: loc / attn above hold sampling offsets / attention logits,
+    // grad_loc / grad_attn receive grad_offsets / grad_logits
+    const void* ref;       // reference points [B, Q, L, 2]
+    int gbuf_off;          // fused backward: byte offset of the per-sample <g, sampled> buffer in shared memory
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -456,6 +460,14 @@ __device__ __forceinline__ void read_params(const KernelArgs& a, const unsigned 
     }
 }
 
+template <typename T>
+__device__ __forceinline__ float read_weight(const KernelArgs& a, const unsigned char* sm, bool staged, int team,
+                                             uint32_t u, int s) {
+    if (staged)
+        return Elem<T>::to_f(reinterpret_cast<const T*>(sm + attn_chunk_offset<T>(a))[team * a.LK + s]);
+    return ldg_f(reinterpret_cast<const T*>(a.attn) + (long long)u * a.LK + s);
+}
+
 // Team geometry of this thread.
 struct Lane {
     int C, P, TP, team, c, p;
@@ -781,7 +793,40 @@ __device__ __forceinline__ int team_lane(const Lane& ln, int c, int p) {
     return ((threadIdx.x & 31) & ~(ln.TP - 1)) + c + p * kC;
 }
 
-template <typename T, int NV>
+// Fused operator (msda-triton README, "The operator": softmax-normalised
+// weights over the L*K (level, point) pairs, locations = reference point plus
+// offset).  Offsets are in pixels of the sample's level: loc = ref + off / W
+// (x) and ref + off / H (y), one binary32 rounding per operation.
+
+// max and sum of exp(logit - max) over the unit's L*K logits, reduced over
+// the team (all lanes of the warp take part; inactive teams get (0, 1))
+template <typename T>
+__device__ __forceinline__ void softmax_stats(const KernelArgs& a, const unsigned char* sm, bool staged,
+                                              const Lane& ln, float& mx, float& sum) {
+    const int lt = ln.c + ln.p * ln.C;
+    float m = -INFINITY;
+    if (ln.active)
+        for (int s = lt; s < a.LK; s += ln.TP) m = fmaxf(m, read_weight<T>(a, sm, staged, ln.team, ln.u, s));
+    for (int o = 1; o < ln.TP; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float t = 0.f;
+    if (ln.active)
+        for (int s = lt; s < a.LK; s += ln.TP) t += expf(read_weight<T>(a, sm, staged, ln.team, ln.u, s) - m);
+    for (int o = 1; o < ln.TP; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    mx = ln.active ? m : 0.f;
+    sum = ln.active ? t : 1.f;
+}
+
+// location of a fused sample from its offset (x, y in pixels) and the
+// reference point of (b*Q + q, level l)
+template <typename T>
+__device__ __forceinline__ void fused_location(const KernelArgs& a, uint32_t bq, int l, const Level& lev, float& x,
+                                               float& y) {
+    const T* rp = reinterpret_cast<const T*>(a.ref) + ((long long)bq * a.L + l) * 2;
+    x = __fadd_rn(ldg_f(rp), __fdiv_rn(x, lev.fW));
+    y = __fadd_rn(ldg_f(rp + 1), __fdiv_rn(y, lev.fH));
+}
+
+template <typename T, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
     using S_ = Slot<T, EPV>;
@@ -800,6 +845,8 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
     const uint32_t m = ln.u - fdiv(ln.u, a.div_m) * (uint32_t)a.M;
     const T* vbase = reinterpret_cast<const T*>(a.value) + (long long)b * a.slice + (long long)m * a.D + ln.c * EPV;
     const int MD = a.M * a.D;
+    float smx = 0.f, ssum = 1.f;
+    if constexpr (FUSED) softmax_stats<T>(a, sm, staged, ln, smx, ssum);
 
     float acc[NV][EPV];
 #pragma unroll
@@ -819,6 +866,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
         }
         Level lev = lv[l];
         if (!live) lev.ok = 0;
+        if constexpr (FUSED) {
+            if (live) {
+                fused_location<T>(a, fdiv(ln.u, a.div_m), l, lev, x, y);
+                w = expf(w - smx) / ssum;
+            }
+        }
         SampleSetup me = sample_setup(lev, x, y, MD);
         float mw[4];
         corner_weights(me.lx, me.ly, mw);
@@ -878,7 +931,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
 // zero kernel, griddepcontrol.wait before the first scatter lets the gather
 // phase of the first round overlap the zeroing of grad_value; launched
 // normally, the wait returns at once.
-template <typename T, typename ACC, int NV>
+template <typename T, typename ACC, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
     using S_ = Slot<T, EPV>;
@@ -915,6 +968,9 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
     T* ga = reinterpret_cast<T*>(a.grad_attn);
     bool waited = false;
     float dscale = 0.f;  // deterministic accumulator: 2^F, read after the wait
+    float smx = 0.f, ssum = 1.f, pdot = 0.f;
+    if constexpr (FUSED) softmax_stats<T>(a, sm, staged, ln, smx, ssum);
+    float* gbuf = reinterpret_cast<float*>(sm + a.gbuf_off) + ln.team * a.LK;  // fused: <g, sampled> per sample
 
     for (int r0 = 0; r0 < a.LK; r0 += ln.TP) {
         const int s_own = r0 + ln.p + ln.c * ln.P;
@@ -927,6 +983,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
         }
         Level lev = lv[l];
         if (!live) lev.ok = 0;
+        if constexpr (FUSED) {
+            if (live) {
+                fused_location<T>(a, fdiv(ln.u, a.div_m), l, lev, x, y);
+                wa = expf(wa - smx) / ssum;
+            }
+        }
         const SampleSetup me = sample_setup(lev, x, y, MD);
 
         // gather + reduce: the lane with c == j keeps the totals of sample j
@@ -983,9 +1045,17 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
         }
         if (live) {
             const long long ps = (long long)ln.u * a.LK + s_own;
-            ga[ps] = Elem<T>::from_f(ra);
-            gl[2 * ps] = Elem<T>::from_f(wa * lev.fW * rx);
-            gl[2 * ps + 1] = Elem<T>::from_f(wa * lev.fH * ry);
+            if constexpr (FUSED) {
+                // d loc / d offset = (1/W, 1/H): the level size cancels
+                gl[2 * ps] = Elem<T>::from_f(wa * rx);
+                gl[2 * ps + 1] = Elem<T>::from_f(wa * ry);
+                gbuf[s_own] = ra;
+                pdot += wa * ra;
+            } else {
+                ga[ps] = Elem<T>::from_f(ra);
+                gl[2 * ps] = Elem<T>::from_f(wa * lev.fW * rx);
+                gl[2 * ps + 1] = Elem<T>::from_f(wa * lev.fH * ry);
+            }
         }
 
         // scatter: A * w_corner * g into the inside corners
@@ -1020,6 +1090,18 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                     else
                         Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
                 }
+            }
+        }
+    }
+    if constexpr (FUSED) {
+        // softmax backward: grad_logit_s = A_s * (<g, sampled_s> - sum_j A_j <g, sampled_j>)
+        for (int o = 1; o < ln.TP; o <<= 1) pdot += __shfl_xor_sync(0xffffffffu, pdot, o);
+        __syncwarp();
+        for (int r0 = 0; r0 < a.LK; r0 += ln.TP) {
+            const int s_own = r0 + ln.p + ln.c * ln.P;
+            if (ln.active && s_own < a.LK) {
+                const float A = expf(read_weight<T>(a, sm, staged, ln.team, ln.u, s_own) - smx) / ssum;
+                ga[(long long)ln.u * a.LK + s_own] = Elem<T>::from_f(A * (gbuf[s_own] - pdot));
             }
         }
     }
@@ -1270,6 +1352,29 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd_pointparallel_kernel(c
 }
 
 // ---------------------------------------------------------------------------
+// fused operator: gradient of the reference points, d loc / d ref = 1:
+// grad_ref[bq, l, c] = sum over (m, k) of grad_loc = grad_offsets * (W_l | H_l)
+
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_fused_ref_grad_kernel(const T* goff, T* gref,
+                                                                            const int64_t* shapes, long long BQ,
+                                                                            int M, int L, int K) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= BQ * L * 2) return;
+    const int c = (int)(i & 1);
+    const int l = (int)((i >> 1) % L);
+    const long long bq = (i >> 1) / L;
+    const long long side = shapes[2 * l + (c == 0 ? 1 : 0)];   // W for x, H for y
+    const float scale = (side >= 1 && side <= kMaxSide) ? (float)side : 0.f;
+    float acc = 0.f;
+    for (int m = 0; m < M; ++m) {
+        const T* p = goff + ((((bq * M + m) * L + l) * (long long)K) * 2) + c;
+        for (int k = 0; k < K; ++k) acc += Elem<T>::to_f(p[2 * k]) * scale;
+    }
+    gref[i] = Elem<T>::from_f(acc);
+}
+
+// ---------------------------------------------------------------------------
 // deterministic accumulator: maxima and conversion
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -1279,16 +1384,17 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // max |g| and max |A| into the header (order-free: atomicMax on the bits of
-// non-negative floats; NaN compares false and is skipped)
+// non-negative floats; NaN compares false and is skipped).  max |A| starts at
+// ma0: 1 for softmax-normalised weights, which then need no scan (na = 0).
 template <typename T>
 __global__ void __launch_bounds__(kBlockThreads) msda_det_max_kernel(const T* g, long long ng, const T* attn,
-                                                                     long long na, DetHeader* h) {
+                                                                     long long na, float ma0, DetHeader* h) {
     // the backward (a programmatic dependent) may start its gather phase now
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float red[2][kBlockThreads / 32];
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nth = (long long)gridDim.x * blockDim.x;
-    float mg = 0.f, ma = 0.f;
+    float mg = 0.f, ma = ma0;
     for (long long i = tid; i < ng; i += nth) mg = fmaxf(mg, fabsf(Elem<T>::to_f(g[i])));
     for (long long i = tid; i < na; i += nth) ma = fmaxf(ma, fabsf(Elem<T>::to_f(attn[i])));
     mg = warp_max(mg);

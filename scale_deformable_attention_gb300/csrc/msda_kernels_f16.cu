@@ -11,7 +11,8 @@ template void launch_backward<__half, float>(const KernelArgs&, const Plan&, cud
 template void launch_convert<__half>(const float*, __half*, long long, int, int, cudaStream_t);
 template void launch_widen<__half>(const __half*, float*, long long, int, cudaStream_t);
 template void launch_backward<__half, long long>(const KernelArgs&, const Plan&, cudaStream_t);
-template void launch_det_max<__half>(const __half*, long long, const __half*, long long, DetHeader*, int, cudaStream_t);
+template void launch_det_max<__half>(const __half*, long long, const __half*, long long, float, DetHeader*, int, cudaStream_t);
 template void launch_det_convert<__half>(const long long*, __half*, long long, const DetHeader*, long long, int, int,
                                       cudaStream_t);
+template void launch_fused_ref_grad<__half>(const __half*, __half*, const int64_t*, long long, int, int, int, cudaStream_t);
 }  // namespace msda

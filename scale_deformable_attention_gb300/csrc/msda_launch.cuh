@@ -19,6 +19,7 @@ struct Plan {
     bool wide;     // 64-bit offsets inside a batch slice
     bool spec;     // specialised kernels: C = 4, nvec == 4 * nv, nv <= 3, 32-bit offsets
     bool pdl;      // backward launched as a programmatic dependent of the zero kernel
+    bool fused;    // fused operator (offsets + logits in, offset / logit gradients out)
 };
 
 #define MSDA_DISPATCH_NV(NVV, ...)                                   \
@@ -48,11 +49,12 @@ static void bwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
 
 template <typename T, int NV>
 static void fwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
-    msda_fwd4_kernel<T, NV><<<pl.grid, pl.block, pl.smem, st>>>(a);
+    if (pl.fused) msda_fwd4_kernel<T, NV, true><<<pl.grid, pl.block, pl.smem, st>>>(a);
+    else msda_fwd4_kernel<T, NV, false><<<pl.grid, pl.block, pl.smem, st>>>(a);
 }
 
-template <typename T, typename ACC, int NV>
-static void bwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+template <typename T, typename ACC, int NV, bool FUSED>
+static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     if (pl.pdl) {
         // may start while the zero kernel that precedes it still runs; the
         // kernel waits (griddepcontrol.wait) before its first scatter
@@ -66,10 +68,16 @@ static void bwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
         at[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, msda_bwd4_kernel<T, ACC, NV>, a);
+        cudaLaunchKernelEx(&cfg, msda_bwd4_kernel<T, ACC, NV, FUSED>, a);
     } else {
-        msda_bwd4_kernel<T, ACC, NV><<<pl.grid, pl.block, pl.smem, st>>>(a);
+        msda_bwd4_kernel<T, ACC, NV, FUSED><<<pl.grid, pl.block, pl.smem, st>>>(a);
     }
+}
+
+template <typename T, typename ACC, int NV>
+static void bwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    if (pl.fused) bwd4_go2<T, ACC, NV, true>(a, pl, st);
+    else bwd4_go2<T, ACC, NV, false>(a, pl, st);
 }
 
 template <typename T>
@@ -123,8 +131,17 @@ void launch_forward_pointparallel(const KernelArgs& a, unsigned grid, cudaStream
 }
 
 template <typename T>
-void launch_det_max(const T* g, long long ng, const T* attn, long long na, DetHeader* h, int grid, cudaStream_t st) {
-    msda_det_max_kernel<T><<<grid, kBlockThreads, 0, st>>>(g, ng, attn, na, h);
+void launch_fused_ref_grad(const T* goff, T* gref, const int64_t* shapes, long long BQ, int M, int L, int K,
+                           cudaStream_t st) {
+    const long long n = BQ * L * 2;
+    msda_fused_ref_grad_kernel<T><<<(unsigned)((n + kBlockThreads - 1) / kBlockThreads), kBlockThreads, 0, st>>>(
+        goff, gref, shapes, BQ, M, L, K);
+}
+
+template <typename T>
+void launch_det_max(const T* g, long long ng, const T* attn, long long na, float ma0, DetHeader* h, int grid,
+                    cudaStream_t st) {
+    msda_det_max_kernel<T><<<grid, kBlockThreads, 0, st>>>(g, ng, attn, na, ma0, h);
 }
 
 template <typename T>
@@ -149,9 +166,11 @@ void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st
     extern template void launch_forward<T>(const KernelArgs&, const Plan&, cudaStream_t); \
     extern template void launch_forward_tma<T>(const KernelArgs&, const CUtensorMap&, int, unsigned, cudaStream_t); \
     extern template void launch_forward_pointparallel<T>(const KernelArgs&, unsigned, cudaStream_t); \
+    extern template void launch_fused_ref_grad<T>(const T*, T*, const int64_t*, long long, int, int, int, cudaStream_t); \
     extern template void launch_backward<T, float>(const KernelArgs&, const Plan&, cudaStream_t);             \
     extern template void launch_backward<T, long long>(const KernelArgs&, const Plan&, cudaStream_t);         \
-    extern template void launch_det_max<T>(const T*, long long, const T*, long long, DetHeader*, int, cudaStream_t); \
+    extern template void launch_det_max<T>(const T*, long long, const T*, long long, float, DetHeader*, int,    \
+                                           cudaStream_t);                                                         \
     extern template void launch_det_convert<T>(const long long*, T*, long long, const DetHeader*, long long, int, int, \
                                                cudaStream_t);
 MSDA_EXTERN_IO(float)

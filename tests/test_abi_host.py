@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("msda_forward", "msda_backward", "msda_backward_workspace_size", "msda_last_error",
-              "msda_resolve_accum", "msda_device_errors", "msda_trace_enable", "msda_trace_read"):
+              "msda_resolve_accum", "msda_device_errors", "msda_trace_enable", "msda_trace_read",
+              "msda_forward_fused", "msda_backward_fused", "msda_backward_static_workspace"):
         assert n in names
 
 
@@ -46,6 +47,24 @@ def test_library_exports_every_declared_function(lib):
     assert not missing, f"declared but not exported: {missing}"
     for n in declared_functions():
         assert hasattr(lib, n)
+
+
+def declared_arity():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(msda_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_argtypes_match_the_header(lib):
+    arity = declared_arity()
+    assert "msda_backward_fused" in arity
+    for name, n in arity.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is not None:
+            assert len(fn.argtypes) == n, f"{name}: header has {n} parameters, binding declares {len(fn.argtypes)}"
 
 
 F32, F16, BF16 = 0, 1, 2
@@ -162,6 +181,53 @@ def test_workspace_size_and_resolution(lib):
     # many samples per pixel: bf16 AUTO goes to the fp32 accumulator
     dense = (2, 22223, 8, 32, 4, 4, 22223)
     assert lib.msda_resolve_accum(BF16, 0, *dense) == 2
+
+
+def fused_fwd(lib, dt=F32, ptrs=None, **kw):
+    d = dict(GOOD)
+    d.update(kw)
+    p = [FAKE] * 7 if ptrs is None else ptrs
+    return lib.msda_forward_fused(dt, d["B"], d["S"], d["M"], d["D"], d["L"], d["K"], d["Q"], *p, None)
+
+
+def fused_bwd(lib, dt=F32, mode=0, flags=0, ptrs=None, **kw):
+    d = dict(GOOD)
+    d.update(kw)
+    p = [FAKE] * 11 if ptrs is None else ptrs
+    return lib.msda_backward_fused(dt, mode, flags, d["B"], d["S"], d["M"], d["D"], d["L"], d["K"], d["Q"], *p,
+                                   None, 0, None)
+
+
+@pytest.mark.parametrize("idx,name", [(0, "value"), (3, "reference_points"), (4, "sampling_offsets"),
+                                      (5, "attention_logits"), (6, "out")])
+def test_fused_forward_rejects_null(lib, idx, name):
+    p = [FAKE] * 7
+    p[idx] = None
+    assert fused_fwd(lib, ptrs=p) == 1
+    assert name in msg(lib) and "NULL" in msg(lib)
+
+
+@pytest.mark.parametrize("idx,name", [(3, "reference_points"), (4, "sampling_offsets"), (5, "attention_logits"),
+                                      (6, "grad_out"), (7, "grad_value"), (8, "grad_reference_points"),
+                                      (9, "grad_sampling_offsets"), (10, "grad_attention_logits")])
+def test_fused_backward_rejects_null(lib, idx, name):
+    p = [FAKE] * 11
+    p[idx] = None
+    assert fused_bwd(lib, ptrs=p) == 1
+    assert name in msg(lib) and "NULL" in msg(lib)
+
+
+def test_fused_rejects_sizes_and_modes(lib):
+    assert fused_fwd(lib, K=65) == 2 and "K=65" in msg(lib)
+    assert fused_bwd(lib, mode=9) == 1 and "accumulator" in msg(lib)
+    assert fused_bwd(lib, dt=BF16, mode=3) == 4 and "deterministic" in msg(lib)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Q=0)])
+def test_fused_empty_is_ok_without_launch(lib, kw):
+    assert fused_fwd(lib, ptrs=[None] * 7, **kw) == 0
+    if "B" in kw:  # nothing to zero either
+        assert fused_bwd(lib, ptrs=[None] * 11, **kw) == 0
 
 
 def test_status_strings_version_kernel_names(lib):
