@@ -48,23 +48,41 @@ FALLBACK_HBM_GBS = 6800.0
 # ---------------------------------------------------------------------------
 # byte model (algorithmic bytes per launch)
 
-def inbounds_corners(wl: W.Workload, inp) -> int:
-    """Number of (sample, corner) pairs whose corner lies inside its level, on
-    the binary32 pixel coordinate the kernels use."""
-    loc = W.to_f64(inp["sampling_locations"], wl.dtype)
+def corner_counts(wl: W.Workload, inp, unique: bool = True):
+    """(in-bounds (sample, corner) pairs, distinct value rows they touch), on
+    the binary32 pixel coordinate the kernels use.  A value row is one
+    (b, pixel, m): D contiguous channels."""
+    loc = W.to_f64(inp["sampling_locations"], wl.dtype)         # [B,Q,M,L,K,2]
+    B, Q, M = loc.shape[:3]
+    starts = W.level_start_index(wl.shapes)
+    b_idx = np.arange(B, dtype=np.int64)[:, None, None, None]
+    m_idx = np.arange(M, dtype=np.int64)[None, None, :, None]
     n = 0
+    rows = []
     for l, (h, w) in enumerate(wl.shapes):
         # exact in fp64 for binary32 inputs and sides <= 8192, then one rounding
-        x = np.floor((loc[:, :, :, l, :, 0] * w - 0.5).astype(np.float32))
-        y = np.floor((loc[:, :, :, l, :, 1] * h - 0.5).astype(np.float32))
+        x = np.floor((loc[:, :, :, l, :, 0] * w - 0.5).astype(np.float32)).astype(np.int64)
+        y = np.floor((loc[:, :, :, l, :, 1] * h - 0.5).astype(np.float32)).astype(np.int64)
         for dy in (0, 1):
             for dx in (0, 1):
                 xx, yy = x + dx, y + dy
-                n += int(np.count_nonzero((xx >= 0) & (xx < w) & (yy >= 0) & (yy < h)))
-    return n
+                ok = (xx >= 0) & (xx < w) & (yy >= 0) & (yy < h)
+                n += int(np.count_nonzero(ok))
+                if unique:
+                    r = ((b_idx * wl.S + starts[l] + yy * w + xx) * M + m_idx)
+                    rows.append(np.unique(r[ok]))
+    u = int(np.unique(np.concatenate(rows)).size) if unique and rows else None
+    return n, u
 
 
-def byte_model(wl: W.Workload, corners: int) -> dict:
+def inbounds_corners(wl: W.Workload, inp) -> int:
+    return corner_counts(wl, inp, unique=False)[0]
+
+
+def byte_model(wl: W.Workload, corners: int, unique_rows=None) -> dict:
+    """Algorithmic bytes per launch.  Per-corner model: every in-bounds corner
+    row counted each time it is read (and, in the backward, written by a
+    reduction).  Unique (compulsory) model: each distinct value row once."""
     es = W.ESIZE[wl.dtype]
     n_value = wl.B * wl.S * wl.M * wl.D
     loc = wl.samples * 2 * es
@@ -75,8 +93,14 @@ def byte_model(wl: W.Workload, corners: int) -> dict:
     # backward kernel: corner reads + atomic payload at the value dtype, grad_out, params, param grads
     bwd_kernel = 2 * gather + rowio + 2 * (loc + attn)
     bwd = bwd_kernel + n_value * es          # + one full grad_value write
-    return {"forward": fwd, "backward": bwd_kernel, "bwd_total": bwd, "zero": n_value * es,
-            "convert": n_value * (4 + es), "step": fwd + bwd}
+    out = {"forward": fwd, "backward": bwd_kernel, "bwd_total": bwd, "zero": n_value * es,
+           "convert": n_value * (4 + es), "step": fwd + bwd}
+    if unique_rows is not None:
+        urow = unique_rows * wl.D * es
+        out["unique_rows"] = unique_rows
+        out["forward_unique"] = urow + loc + attn + rowio
+        out["bwd_total_unique"] = urow + rowio + 2 * (loc + attn) + n_value * es
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -286,6 +310,21 @@ def job_throughput(units_per_rank: int, world: int, steps: int, total_ms: float)
     return units_per_rank * world * steps / (total_ms / 1e3)
 
 
+def unique_fractions(model: dict, kernels: dict, peak: float):
+    """Compulsory-byte (unique value rows) fractions of the measured peak for
+    the traced forward and backward (zero + kernel + convert) durations."""
+    if "forward_unique" not in model or "forward" not in kernels or "backward" not in kernels:
+        return None
+    tf = kernels["forward"]["avg_ms"]
+    tb = sum(kernels[k]["avg_ms"] * kernels[k]["launches"] / kernels["backward"]["launches"]
+             for k in ("zero", "backward", "convert") if k in kernels)
+    return {"unique_rows": model["unique_rows"], "forward_bytes": model["forward_unique"],
+            "backward_bytes": model["bwd_total_unique"],
+            "forward_frac": round(model["forward_unique"] / (tf / 1e3) / 1e9 / peak, 4),
+            "backward_frac": round(model["bwd_total_unique"] / (tb / 1e3) / 1e9 / peak, 4),
+            "peak": peak, "unit": "GB/s"}
+
+
 def run_ours(args):
     import torch
 
@@ -301,8 +340,8 @@ def run_ours(args):
     inp = W.make_inputs(wl)
     accum = args.accum or wl.accum
     st = GpuStep(wl, inp, accum, device)
-    corners = inbounds_corners(wl, inp)
-    model = byte_model(wl, corners)
+    corners, urows = corner_counts(wl, inp)
+    model = byte_model(wl, corners, urows)
 
     for _ in range(max(args.warmup, 3)):
         st.flush()
@@ -362,6 +401,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
             "roofline": roof, "kernels": kernels, "bytes_per_step_model": model["step"],
+            "unique_model": unique_fractions(model, kernels, peak),
             "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
             "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "traced_steps_every": args.trace_every,
         }
@@ -474,8 +514,8 @@ def run_workload_table(name: str, args, device):
     inp = W.make_inputs(wl)
     out = {}
     accums = ["native", "fp32", "deterministic"] if wl.dtype != "f32" else ["auto", "deterministic"]
-    corners = inbounds_corners(wl, inp)
-    model = byte_model(wl, corners)
+    corners, urows = corner_counts(wl, inp)
+    model = byte_model(wl, corners, urows)
     peak, _ = peaks()
     for accum in accums:
         st = GpuStep(wl, inp, accum, device)
@@ -492,7 +532,11 @@ def run_workload_table(name: str, args, device):
                       "fwd_frac_of_8TBs": round(model["forward"] / (tf / 1e3) / 8e12, 4),
                       "bwd_frac_of_8TBs": round(model["bwd_total"] / (tb / 1e3) / 8e12, 4),
                       "fwd_frac_of_measured": round(model["forward"] / (tf / 1e3) / 1e9 / peak, 4),
-                      "bwd_frac_of_measured": round(model["bwd_total"] / (tb / 1e3) / 1e9 / peak, 4)}
+                      "bwd_frac_of_measured": round(model["bwd_total"] / (tb / 1e3) / 1e9 / peak, 4),
+                      "fwd_unique_frac_of_8TBs": round(model["forward_unique"] / (tf / 1e3) / 8e12, 4),
+                      "bwd_unique_frac_of_8TBs": round(model["bwd_total_unique"] / (tb / 1e3) / 8e12, 4),
+                      "fwd_unique_frac_of_measured": round(model["forward_unique"] / (tf / 1e3) / 1e9 / peak, 4),
+                      "bwd_unique_frac_of_measured": round(model["bwd_total_unique"] / (tb / 1e3) / 1e9 / peak, 4)}
         del st
         torch.cuda.empty_cache()
     return {"table": name, "units": wl.units, "corners_inside": corners, "bytes_model": model, "results": out}
