@@ -227,7 +227,7 @@ void pick_c(int nvec, int* C, int* NV) {
 }
 
 msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool backward, const void* loc,
-                      const void* attn, Plan& pl, KernelArgs& a, bool fused = false) {
+                      const void* attn, Plan& pl, KernelArgs& a, bool fused = false, int lane_scale = 1) {
     const int es = (int)esize(dt);
     const int epv = vec ? 16 / es : 1;
     const int nvec = (int)(d.D / epv);
@@ -244,10 +244,12 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     }
     // point lanes: enough lanes to fill the GPU, within one warp (C*P <= 32)
     // and L*K.  Measured on GB300: ~768 lanes per SM (one resident wave at
-    // these register counts) for both kernels, and at least two point lanes
-    // per unit for the backward.
+    // these register counts) for both kernels, at least two point lanes per
+    // unit for the backward, and twice the lanes for a forward whose gathers
+    // come from DRAM (value larger than the L2: more loads in flight; odd-D
+    // fp32 forward 108 -> 91 us).
     int P = 1;
-    const int64_t target = (int64_t)sms * 768;
+    const int64_t target = (int64_t)sms * 768 * lane_scale;
     while (P * C < 32 && P * 2 <= LK && d.units * C * P < target) P *= 2;
     if (backward && P == 1 && C < 32 && LK >= 2) P = 2;
     if (t.P > 0 && (t.P & (t.P - 1)) == 0 && t.P * C <= 32) P = t.P;
@@ -580,9 +582,11 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
     DeviceInfo* di = nullptr;
     if ((s = device_info(&di))) return s;
     const bool vec = (d.D * (int64_t)es) % 16 == 0 && aligned(value, 16) && aligned(out, 16);
+    // value larger than the L2: the gathers are served by DRAM
+    const bool big = d.n_value * (int64_t)es > (int64_t)di->l2_bytes;
     KernelArgs a{};
     Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, false, loc, attn, pl, a, ref != nullptr))) return s;
+    if ((s = make_plan(dt, d, vec, di->sms, false, loc, attn, pl, a, ref != nullptr, big ? 2 : 1))) return s;
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;
@@ -591,16 +595,18 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
     a.out = out;
     a.err = di->err;
     a.ref = ref;
-    // TMA-gather forward: whole 16-byte rows, L*K in {4, 8, 16, 32}, row
-    // coordinates of the [B*S*M, D] view below 2^31, and a value tensor
+    // TMA-gather forward: whole 16-byte rows of one slot per channel lane
+    // (64-byte rows of bf16/fp16 D=32, fp32 D=16), L*K in {4, 8, 16, 32},
+    // row coordinates of the [B*S*M, D] view below 2^31, and a value tensor
     // larger than the L2.  Measured on GB300: with value far above the L2
     // (gathers served by DRAM) the gathers are faster than 16-byte loads
     // (stress workload forward -24%); with value inside the L2 the load path
-    // is faster (encoder workload forward +59% with gathers).
+    // is faster (encoder workload forward +59% with gathers); with 192-byte
+    // rows the staged corners limit a block to 12% occupancy and the load
+    // path is faster (odd-D fp32 forward 107 us with gathers, 91 us without).
     const int LK = (int)(d.L * d.K);
-    const bool big = d.n_value * (int64_t)es > (int64_t)di->l2_bytes;
     CUtensorMap map;
-    const bool tma = !ref && pl.spec && !tune().notma && (big || tune().tma) &&
+    const bool tma = !ref && pl.spec && pl.nv == 1 && !tune().notma && (big || tune().tma) &&
                      (LK == 4 || LK == 8 || LK == 16 || LK == 32) && d.B * d.S * d.M < (1ll << 31) &&
                      value_tensor_map(dt, value, d.B * d.S * d.M, d.D, &map);
     TraceScope ts(st);

@@ -788,6 +788,14 @@ __device__ __forceinline__ float dot2(const float (&g)[EPV], const float (&v)[EP
     return t.x + t.y;
 }
 
+// Samples whose corners a lane loads in one batch before using them.
+// Measured on GB300: two beats one for every slot count, even at three
+// 16-byte slots per lane, where it doubles the registers (fp32 D=48
+// backward 211 us at 126 registers vs 248 us at 60): loads in flight per
+// lane matter more than occupancy here.
+template <int NV>
+constexpr int kGatherBatch = 2;
+
 // Lane index (within the warp) of lane (c, p) of this thread's team.
 __device__ __forceinline__ int team_lane(const Lane& ln, int c, int p) {
     return ((threadIdx.x & 31) & ~(ln.TP - 1)) + c + p * kC;
@@ -829,6 +837,7 @@ __device__ __forceinline__ void fused_location(const KernelArgs& a, uint32_t bq,
 template <typename T, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
+    constexpr int JB = kGatherBatch<NV>;
     using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
@@ -880,11 +889,11 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
         for (int k = 0; k < 4; ++k) mc[k] = ((me.mask >> k) & 1u) ? w * mw[k] : 0.f;
 
 #pragma unroll
-        for (int j0 = 0; j0 < kC; j0 += 2) {
-            typename S_::Raw raw[2][4][NV];
-            float cf[2][4];
+        for (int j0 = 0; j0 < kC; j0 += JB) {
+            typename S_::Raw raw[JB][4][NV];
+            float cf[JB][4];
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
+            for (int jj = 0; jj < JB; ++jj) {
                 const int src = team_lane(ln, j0 + jj, ln.p);
                 const int o = __shfl_sync(0xffffffffu, me.o, src);
                 const int wmd = __shfl_sync(0xffffffffu, me.wmd, src);
@@ -899,7 +908,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
                         raw[jj][k][n] = ((mask >> k) & 1u) ? S_::load_raw(vbase + off[k] + n * kC * EPV) : S_::zero();
             }
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
+            for (int jj = 0; jj < JB; ++jj)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
@@ -934,6 +943,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
 template <typename T, typename ACC, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
+    constexpr int JB = kGatherBatch<NV>;
     using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
@@ -994,11 +1004,11 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
         // gather + reduce: the lane with c == j keeps the totals of sample j
         float ra = 0.f, rx = 0.f, ry = 0.f;
 #pragma unroll
-        for (int j0 = 0; j0 < kC; j0 += 2) {
-            typename S_::Raw raw[2][4][NV];
-            SampleSetup st[2];
+        for (int j0 = 0; j0 < kC; j0 += JB) {
+            typename S_::Raw raw[JB][4][NV];
+            SampleSetup st[JB];
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
+            for (int jj = 0; jj < JB; ++jj) {
                 st[jj] = shfl_setup(me, team_lane(ln, j0 + jj, ln.p));
                 const int off[4] = {st[jj].o, st[jj].o + MD, st[jj].o + st[jj].wmd, st[jj].o + st[jj].wmd + MD};
 #pragma unroll
@@ -1009,7 +1019,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                                                                   : S_::zero();
             }
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
+            for (int jj = 0; jj < JB; ++jj) {
                 float d[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
