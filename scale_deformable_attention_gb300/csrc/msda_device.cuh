@@ -789,12 +789,15 @@ __device__ __forceinline__ float dot2(const float (&g)[EPV], const float (&v)[EP
 }
 
 // Samples whose corners a lane loads in one batch before using them.
-// Measured on GB300: two beats one for every slot count, even at three
-// 16-byte slots per lane, where it doubles the registers (fp32 D=48
-// backward 211 us at 126 registers vs 248 us at 60): loads in flight per
-// lane matter more than occupancy here.
+// Measured on GB300: in the forward, all four samples of a round for one
+// 16-byte slot per lane (encoder forward 122 -> 111 us), else two; in the
+// backward, two for every slot count: four slowed the encoder backward
+// (344 -> 367 us), and one halved the registers at three slots but slowed
+// the fp32 D=48 backward (211 -> 248 us).  Loads in flight per lane matter
+// more than occupancy here.
 template <int NV>
-constexpr int kGatherBatch = 2;
+constexpr int kGatherBatchFwd = NV == 1 ? 4 : 2;
+constexpr int kGatherBatchBwd = 2;
 
 // Lane index (within the warp) of lane (c, p) of this thread's team.
 __device__ __forceinline__ int team_lane(const Lane& ln, int c, int p) {
@@ -837,7 +840,7 @@ __device__ __forceinline__ void fused_location(const KernelArgs& a, uint32_t bq,
 template <typename T, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
-    constexpr int JB = kGatherBatch<NV>;
+    constexpr int JB = kGatherBatchFwd<NV>;
     using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
@@ -943,7 +946,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
 template <typename T, typename ACC, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
-    constexpr int JB = kGatherBatch<NV>;
+    constexpr int JB = kGatherBatchBwd;
     using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
