@@ -131,6 +131,7 @@ struct Tune {
     bool notma = false;    // no TMA-gather forward
     bool tma = false;      // TMA-gather forward whatever the size
     bool pointparallel = false;  // the point-parallel ablation forward (D = 32 only)
+    bool pdl = true;       // forward and zero kernel as programmatic dependents (off: nopdl)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -149,6 +150,7 @@ const Tune& tune() {
             else if (!strcmp(tok, "notma")) r.notma = true;
             else if (!strcmp(tok, "tma")) r.tma = true;
             else if (!strcmp(tok, "pointparallel")) r.pointparallel = true;
+            else if (!strcmp(tok, "nopdl")) r.pdl = false;
         }
         return r;
     }();
@@ -300,9 +302,11 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     pl.vec = vec;
     pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && NV <= 3 && !t.generic;
     pl.pdl = false;
+    pl.sms = sms;
     pl.fused = fused;
     a.ref = nullptr;
     a.gbuf_off = 0;
+    a.pdl_early = 0;
     if (fused && backward) {
         const int64_t gbuf = (int64_t)tpb * LK * 4;
         int64_t off = mode != msda::PARAMS_DIRECT ? (int64_t)((pl.smem + 15) / 16 * 16) : 0;
@@ -399,8 +403,13 @@ int grid_for(int64_t n, int sms) {
 
 namespace msda {
 __global__ void __launch_bounds__(kBlockThreads) msda_zero_kernel(unsigned char* p, long long nbytes) {
-    // a backward launched as a programmatic dependent may start its gather
-    // phase now; it waits for this grid before its first scatter
+    // Launched as a programmatic dependent, this grid may start before the
+    // kernel ahead of it has finished: wait for it (and its memory) first.
+    // Only then may the backward that depends on this grid start its gather
+    // phase, so that phase never reads inputs an earlier kernel is still
+    // writing; it waits for this grid before its first scatter.  Launched
+    // normally, the wait returns at once.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // head up to 16-byte alignment, 16-byte body, tail
     const uintptr_t addr = reinterpret_cast<uintptr_t>(p);
@@ -424,7 +433,23 @@ msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
     // the SM stays free for a backward that starts early (programmatic launch)
     const int64_t want = nbytes / 16 / msda::kBlockThreads + 1;
     const int grid = (int)(want < 2 * (int64_t)sms ? want : 2 * (int64_t)sms);
-    msda::msda_zero_kernel<<<grid, msda::kBlockThreads, 0, st>>>(static_cast<unsigned char*>(p), nbytes);
+    unsigned char* ptr = static_cast<unsigned char*>(p);
+    if (tune().pdl && !trace_active()) {
+        // may start while the kernel ahead of it runs: it waits for that
+        // kernel before storing, and only then lets its dependents start
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(msda::kBlockThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, msda::msda_zero_kernel, ptr, nbytes);
+    } else {
+        msda::msda_zero_kernel<<<grid, msda::kBlockThreads, 0, st>>>(ptr, nbytes);
+    }
     ts.end(MSDA_KERNEL_ZERO, nbytes);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? MSDA_OK : cuda_fail(e, "zero kernel launch");
@@ -629,6 +654,7 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
         default: msda::launch_forward_tma<__nv_bfloat16>(a, map, pl.nv, grid, st); break;
         }
     } else {
+        pl.pdl = pl.spec && tune().pdl && !trace_active();
         switch (dt) {
         case MSDA_F32: msda::launch_forward<float>(a, pl, st); break;
         case MSDA_F16: msda::launch_forward<__half>(a, pl, st); break;

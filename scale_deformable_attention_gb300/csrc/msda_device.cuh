@@ -96,6 +96,7 @@ struct KernelArgs {
     // grad_loc / grad_attn receive grad_offsets / grad_logits
     const void* ref;       // reference points [B, Q, L, 2]
     int gbuf_off;          // fused backward: byte offset of the per-sample <g, sampled> buffer in shared memory
+    int pdl_early;         // forward: let the next kernel launch at the start (whole grid resident)
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -847,6 +848,17 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
     __shared__ int verdict;
     extern __shared__ __align__(16) unsigned char sm[];
 
+    // Launched as a programmatic dependent, this grid may start before the
+    // kernel ahead of it (which may have written its inputs) has finished:
+    // wait for it before reading anything.  Launched normally, the wait
+    // returns at once.  When the whole grid is resident (one wave), the next
+    // kernel may launch from the start and wait for this grid, which hides
+    // its launch.  With several waves it launches when this grid completes:
+    // its waiting blocks would take the SM slots of the later waves
+    // (measured on GB300: odd-D fp32 step +4% with a trigger at the end of
+    // each block, +15% with one at the start).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (a.pdl_early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Lane ln = lane_of(a);
     if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
         if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);

@@ -4,6 +4,8 @@
 // translation unit (msda_kernels_<dtype>.cu) so they compile in parallel.
 #pragma once
 
+#include <mutex>
+
 #include "msda_device.cuh"
 
 namespace msda {
@@ -18,7 +20,8 @@ struct Plan {
     bool vec;      // 16-byte slots (else one element per slot)
     bool wide;     // 64-bit offsets inside a batch slice
     bool spec;     // specialised kernels: C = 4, nvec == 4 * nv, nv <= 3, 32-bit offsets
-    bool pdl;      // backward launched as a programmatic dependent of the zero kernel
+    bool pdl;      // launched as a programmatic dependent of the kernel ahead of it
+    int sms;       // multiprocessors of the device
     bool fused;    // fused operator (offsets + logits in, offset / logit gradients out)
 };
 
@@ -47,17 +50,12 @@ static void bwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     default: { constexpr int NV = 3; __VA_ARGS__; } break;           \
     }
 
-template <typename T, int NV>
-static void fwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
-    if (pl.fused) msda_fwd4_kernel<T, NV, true><<<pl.grid, pl.block, pl.smem, st>>>(a);
-    else msda_fwd4_kernel<T, NV, false><<<pl.grid, pl.block, pl.smem, st>>>(a);
-}
-
-template <typename T, typename ACC, int NV, bool FUSED>
-static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+// Launch `kernel` with pl's shape; with pl.pdl as a programmatic dependent of
+// the kernel ahead of it on the stream (it may start before that kernel has
+// finished, and must griddepcontrol.wait before touching what it wrote).
+static inline void launch_plan(void (*kernel)(const KernelArgs), const KernelArgs& a, const Plan& pl,
+                               cudaStream_t st) {
     if (pl.pdl) {
-        // may start while the zero kernel that precedes it still runs; the
-        // kernel waits (griddepcontrol.wait) before its first scatter
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = pl.grid;
         cfg.blockDim = pl.block;
@@ -68,10 +66,55 @@ static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
         at[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, msda_bwd4_kernel<T, ACC, NV, FUSED>, a);
+        cudaLaunchKernelEx(&cfg, kernel, a);
     } else {
-        msda_bwd4_kernel<T, ACC, NV, FUSED><<<pl.grid, pl.block, pl.smem, st>>>(a);
+        kernel<<<pl.grid, pl.block, pl.smem, st>>>(a);
     }
+}
+
+// Whether all of `kernel`'s grid is resident at once (one wave), by the
+// occupancy calculator; cached per kernel and shared-memory size.
+static inline bool one_wave(void (*kernel)(const KernelArgs), const Plan& pl) {
+    struct Entry {
+        const void* k;
+        size_t smem;
+        int blocks;
+    };
+    static Entry cache[64];
+    static int n = 0;
+    static std::mutex mu;
+    int per_sm = -1;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < n; ++i)
+            if (cache[i].k == (const void*)kernel && cache[i].smem == pl.smem) per_sm = cache[i].blocks;
+    }
+    if (per_sm < 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (int)(pl.block.x * pl.block.y), pl.smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            per_sm = 0;
+        }
+        std::lock_guard<std::mutex> lk(mu);
+        if (n < 64) cache[n++] = Entry{(const void*)kernel, pl.smem, per_sm};
+    }
+    return (long long)pl.grid.x * pl.grid.y <= (long long)per_sm * pl.sms;
+}
+
+template <typename T, int NV>
+static void fwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    // the kernel waits for the kernel ahead of it before reading anything
+    void (*k)(const KernelArgs) = pl.fused ? msda_fwd4_kernel<T, NV, true> : msda_fwd4_kernel<T, NV, false>;
+    KernelArgs b = a;
+    b.pdl_early = pl.pdl && one_wave(k, pl) ? 1 : 0;
+    launch_plan(k, b, pl, st);
+}
+
+template <typename T, typename ACC, int NV, bool FUSED>
+static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    // with pl.pdl: may start while the zero kernel that precedes it still
+    // runs; the kernel waits (griddepcontrol.wait) before its first scatter
+    launch_plan(msda_bwd4_kernel<T, ACC, NV, FUSED>, a, pl, st);
 }
 
 template <typename T, typename ACC, int NV>
