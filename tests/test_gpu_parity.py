@@ -326,3 +326,43 @@ def test_stress_full_size_sampled():
     rgv = oracle.grad_value_rows(inp, "bf16", rows)
     got = f64(gv.view(n_rows, wl.D)[torch.from_numpy(rows).to(DEV)])
     assert_grad("bf16", got, rgv, "stress grad_value (sampled rows)")
+
+
+@pytest.mark.slow
+def test_stress_nine_batches_element_index_beyond_2_31():
+    """The stress shapes at B=9: B*S*M*D = 2.41e9 elements, so element
+    indices of the last batch pass 2^31 (not only byte offsets).  Batch 0 is
+    built by the workload's generator and copied to all nine batches on the
+    device; every batch must give the same forward and parameter-gradient
+    bits, and the last batch must match the oracle on the one-batch problem
+    (sampled units and grad_value rows)."""
+    msda = _msda()
+    wl1 = W.WORKLOADS["stress_bf16"].with_(B=1)
+    inp = W.make_inputs(wl1)
+    t1 = to_torch(inp, "bf16", DEV)
+    B = 9
+    assert B * wl1.S * wl1.M * wl1.D > 2 ** 31
+
+    def rep(x):
+        return x.expand(B, *x.shape[1:]).contiguous()
+
+    value, loc, attn, g = (rep(t1[k]) for k in ("value", "sampling_locations", "attention_weights", "grad_out"))
+    out = msda.forward(value, t1["spatial_shapes"], t1["level_start_index"], loc, attn)
+    gv, gl, ga = msda.backward(value, t1["spatial_shapes"], t1["level_start_index"], loc, attn, g, accum="fp32")
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], out[B - 1]) and torch.equal(gl[0], gl[B - 1]) and torch.equal(ga[0], ga[B - 1])
+    del value, loc, attn, g
+    rng = np.random.default_rng(9)
+    n1 = wl1.units
+    units = np.unique(np.concatenate([rng.choice(n1, 2000, replace=False), [0, n1 - 1]]))
+    idx = torch.from_numpy(units).to(DEV)
+    assert_forward("bf16", f64(out[B - 1].reshape(n1, wl1.D)[idx]), oracle.forward_units(inp, "bf16", units),
+                   "last batch out (sampled)")
+    rgl, rga = oracle.backward_units(inp, "bf16", units)
+    LK = wl1.L * wl1.K
+    assert_grad("bf16", f64(gl[B - 1].reshape(n1, LK * 2)[idx]), rgl, "last batch grad_loc (sampled)")
+    assert_grad("bf16", f64(ga[B - 1].reshape(n1, LK)[idx]), rga, "last batch grad_attn (sampled)")
+    rows1 = wl1.S * wl1.M
+    rows = np.unique(rng.choice(rows1, 2000, replace=False))
+    got = f64(gv[B - 1].reshape(rows1, wl1.D)[torch.from_numpy(rows).to(DEV)])
+    assert_grad("bf16", got, oracle.grad_value_rows(inp, "bf16", rows), "last batch grad_value (sampled rows)")
