@@ -800,6 +800,16 @@ template <int NV>
 constexpr int kGatherBatchFwd = NV == 1 ? 4 : 2;
 constexpr int kGatherBatchBwd = 2;
 
+// Channels [0, 4) and [16, 20) from p (16-bit elements, 8-byte aligned), as
+// one 16-byte word in that order.
+template <typename T>
+__device__ __forceinline__ uint4 split_load_raw(const T* p) {
+    static_assert(sizeof(T) == 2, "split slots hold 16-bit elements");
+    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(p));
+    const uint2 hi = __ldg(reinterpret_cast<const uint2*>(p + 16));
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+}
+
 // Lane index (within the warp) of lane (c, p) of this thread's team.
 __device__ __forceinline__ int team_lane(const Lane& ln, int c, int p) {
     return ((threadIdx.x & 31) & ~(ln.TP - 1)) + c + p * kC;
@@ -973,17 +983,33 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
     const bool staged = a.param_mode != PARAMS_DIRECT;
     const uint32_t b = fdiv(ln.u, a.div_qm);
     const uint32_t m = ln.u - fdiv(ln.u, a.div_m) * (uint32_t)a.M;
-    const long long vofs = (long long)b * a.slice + (long long)m * a.D + ln.c * EPV;
+    // Lane channels.  A lane owns EPV channels of each group of kC * EPV:
+    // normally the 16-byte slot [c*EPV, c*EPV + EPV).  A 16-bit value
+    // accumulated into the fp32 workspace splits the slot instead: channels
+    // [4c, 4c+4) and [16+4c, 16+4c+4) of the 32-channel group.  Each corner
+    // then takes two 8-byte loads (still one whole sector per four lanes),
+    // and each 16-byte fp32 reduction of a warp instruction lands with those
+    // of the team's other lanes in whole 32-byte sectors; with whole slots,
+    // every instruction half-fills four sectors and the L2 takes twice the
+    // reduction operations.
+    constexpr bool SPLIT = std::is_same<ACC, float>::value && EPV == 8;
+    const int lane_ch = ln.c * (SPLIT ? 4 : EPV);
+    const long long vofs = (long long)b * a.slice + (long long)m * a.D + lane_ch;
     const T* vbase = reinterpret_cast<const T*>(a.value) + vofs;
     ACC* gbase = reinterpret_cast<ACC*>(a.grad_acc) + vofs;
     const int MD = a.M * a.D;
+    auto load_raw = [&](const T* p) -> typename S_::Raw {
+        if constexpr (SPLIT) return split_load_raw(p);
+        else return S_::load_raw(p);
+    };
 
-    // this lane's channel slots of g = grad_out[b, q, m, :]
+    // this lane's channels of g = grad_out[b, q, m, :]
     float g[NV][EPV];
 #pragma unroll
     for (int n = 0; n < NV; ++n) {
         if (ln.active) {
-            S_::load(reinterpret_cast<const T*>(a.grad_out) + (long long)ln.u * a.D + ln.c * EPV + n * kC * EPV, g[n]);
+            const T* go = reinterpret_cast<const T*>(a.grad_out) + (long long)ln.u * a.D + lane_ch + n * kC * EPV;
+            S_::unpack(load_raw(go), g[n]);
         } else {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) g[n][e] = 0.f;
@@ -1030,7 +1056,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
                     for (int n = 0; n < NV; ++n)
-                        raw[jj][k][n] = ((st[jj].mask >> k) & 1u) ? S_::load_raw(vbase + off[k] + n * kC * EPV)
+                        raw[jj][k][n] = ((st[jj].mask >> k) & 1u) ? load_raw(vbase + off[k] + n * kC * EPV)
                                                                   : S_::zero();
             }
 #pragma unroll
@@ -1110,10 +1136,15 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                         t[e] = r.x;
                         t[e + 1] = r.y;
                     }
-                    if constexpr (std::is_same<ACC, long long>::value)
+                    if constexpr (std::is_same<ACC, long long>::value) {
                         det_scatter<EPV>(gbase + off[k] + n * kC * EPV, t, dscale);
-                    else
+                    } else if constexpr (SPLIT) {
+                        float* q = gbase + off[k] + n * kC * EPV;
+                        red_v4_f32(q, t[0], t[1], t[2], t[3]);
+                        red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+                    } else {
                         Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                    }
                 }
             }
         }
