@@ -1015,6 +1015,23 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
             for (int e = 0; e < EPV; ++e) g[n][e] = 0.f;
         }
     }
+    // Deterministic accumulator: its reductions are 8-byte integers, one per
+    // channel.  For them a lane takes channel kC*e + c of each group (a second
+    // copy of g in that order), so the team's four lanes add four adjacent
+    // integers, one whole 32-byte sector, per instruction; in slot order each
+    // instruction would touch a quarter of four sectors.
+    constexpr bool ILV = std::is_same<ACC, long long>::value;
+    float gi[ILV ? NV : 1][ILV ? EPV : 1];
+    long long* ibase = nullptr;
+    if constexpr (ILV) {
+        const T* go = reinterpret_cast<const T*>(a.grad_out) + (long long)ln.u * a.D + ln.c;
+#pragma unroll
+        for (int n = 0; n < NV; ++n)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+                gi[n][e] = ln.active ? Elem<T>::to_f(__ldg(go + n * kC * EPV + kC * e)) : 0.f;
+        ibase = reinterpret_cast<long long*>(a.grad_acc) + (long long)b * a.slice + (long long)m * a.D + ln.c;
+    }
     T* gl = reinterpret_cast<T*>(a.grad_loc);
     T* ga = reinterpret_cast<T*>(a.grad_attn);
     bool waited = false;
@@ -1137,7 +1154,14 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                         t[e + 1] = r.y;
                     }
                     if constexpr (std::is_same<ACC, long long>::value) {
-                        det_scatter<EPV>(gbase + off[k] + n * kC * EPV, t, dscale);
+                        if constexpr (ILV) {
+                            long long* q = ibase + off[k] + n * kC * EPV;
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e)
+                                red_s64(q + kC * e, __float2ll_rn(cf.x * gi[n][e] * dscale));
+                        } else {
+                            det_scatter<EPV>(gbase + off[k] + n * kC * EPV, t, dscale);
+                        }
                     } else if constexpr (SPLIT) {
                         float* q = gbase + off[k] + n * kC * EPV;
                         red_v4_f32(q, t[0], t[1], t[2], t[3]);
