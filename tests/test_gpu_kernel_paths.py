@@ -1,7 +1,8 @@
 """Every kernel family against the oracle, whatever the size heuristics pick:
 the TMA-gather forward, the generic kernels, direct (unstaged) parameter
-loads, and the staged loads without the bulk copy.  Each runs in a child
-process with MSDA_TUNE set."""
+loads, the staged loads without the bulk copy, the backward's same-cell merge
+forced on and off, and ordinary (non-programmatic) launches.  Each runs in a
+child process with MSDA_TUNE set."""
 import os
 import subprocess
 import sys
@@ -12,7 +13,8 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel"])
+@pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel",
+                                  "merge", "nomerge", "nopdl", "merge,P=2"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
