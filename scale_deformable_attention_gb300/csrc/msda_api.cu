@@ -315,7 +315,7 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     // (4*Q*L*K / S; measured: encoder 64 -> backward -19%, odd-D 2.6 -> -1.5%,
     // decoder 0.86 -> +10%)
     const double density = d.S > 0 ? 4.0 * (double)d.Q * (double)LK / (double)d.S : 0.0;
-    a.merge = t.merge >= 0 ? t.merge : (density >= 2.0 ? 1 : 0);
+    pl.merge = t.merge >= 0 ? t.merge != 0 : density >= 2.0;
     if (fused && backward) {
         const int64_t gbuf = (int64_t)tpb * LK * 4;
         int64_t off = mode != msda::PARAMS_DIRECT ? (int64_t)((pl.smem + 15) / 16 * 16) : 0;

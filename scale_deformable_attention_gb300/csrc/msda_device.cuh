@@ -97,7 +97,6 @@ struct KernelArgs {
     const void* ref;       // reference points [B, Q, L, 2]
     int gbuf_off;          // fused backward: byte offset of the per-sample <g, sampled> buffer in shared memory
     int pdl_early;         // forward: let the next kernel launch at the start (whole grid resident)
-    int merge;             // backward: same-cell merge of a point group's samples before the scatter
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -966,8 +965,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
 // zero kernel, griddepcontrol.wait before the first scatter lets the gather
 // phase of the first round overlap the zeroing of grad_value; launched
 // normally, the wait returns at once.
-template <typename T, typename ACC, int NV, bool FUSED>
-__global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
+// MERGE: 0 none, kMergeCells whole cells only, kMergeCorners every shared corner.
+constexpr int kMergeCells = 1;
+constexpr int kMergeCorners = 2;
+
+template <typename T, typename ACC, int NV, bool FUSED, int MERGE>
+__device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
     constexpr int EPV = 16 / sizeof(T);
     constexpr int JB = kGatherBatchBwd;
     using S_ = Slot<T, EPV>;
@@ -1129,13 +1132,26 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
             }
         }
 
-        // Same-cell merge (a.merge, block-uniform).  Samples of the point
-        // group with the same cell and mask (the same four corner rows) add
-        // the same rows: the last of them adds the sum of their coefficients
-        // A * w_k, the others add nothing.  The reductions bound this kernel
-        // when samples cluster: measured on GB300, the encoder backward takes
-        // 19% less time with 17% fewer reductions; with samples spread
-        // uniformly (decoder) nothing merges and the shuffles cost 2 us.
+        // Corner merge (MERGE).  Samples of the point group that add some of
+        // the same rows merge first: each shared row is added once, by the
+        // last sample holding it, with the sum of their coefficients
+        // A * w_k, and the others skip that corner.  A corner merges only
+        // when it is inside the level for both samples, so equal offsets mean
+        // the same row.  Whole cells: samples with the same cell offset and
+        // level width (an equivalence, so every holder is found).  Every
+        // shared corner: also cells that touch, by edge or corner, on a level
+        // at least three pixels wide.  Two cells sharing a corner row are
+        // within one pixel of each other, and for W >= 3 the nine such offsets
+        // are distinct, so every pair holding a row is found (a missed pair
+        // could lose a coefficient: an intermediate sample would absorb it and
+        // then skip the row for a later holder that did not).
+        // The reductions bound this kernel when samples cluster.  Measured on
+        // GB300, encoder backward: native 346 -> 281 us with whole cells
+        // (17% fewer reductions; 306 us with every corner, whose extra
+        // instructions cost more than its extra 12%); fp32 workspace
+        // 601 -> 454 us with every corner (479 with whole cells).  With
+        // uniformly spread samples (decoder) nothing merges and the code
+        // costs ~2 us, so it is compiled only into the merging kernels.
         float mc[4];
         unsigned smask = me.mask;
         {
@@ -1146,7 +1162,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
             for (int k = 0; k < 4; ++k) mc[k] = oc[k] = wa * w0[k];
 #pragma unroll
             for (int jj = 0; jj < kC; ++jj) {
-                if (!a.merge) break;
+                if constexpr (MERGE == 0) break;
                 const int src = team_lane(ln, jj, ln.p);
                 const int o2 = __shfl_sync(0xffffffffu, me.o, src);
                 const int w2 = __shfl_sync(0xffffffffu, me.wmd, src);
@@ -1154,12 +1170,42 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
                 float c2[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) c2[k] = __shfl_sync(0xffffffffu, oc[k], src);
-                const bool same = me.mask != 0u && m2 == me.mask && o2 == me.o && w2 == me.wmd;
-                if (same && jj < ln.c) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) mc[k] += c2[k];
+                if (jj == ln.c || w2 != me.wmd) continue;
+                const bool earlier = jj < ln.c;
+                // my corner k is the other sample's corner k2
+                auto share = [&](int k, int k2) {
+                    if (((me.mask >> k) & 1u) && ((m2 >> k2) & 1u)) {
+                        if (earlier) mc[k] += c2[k2];
+                        else smask &= ~(1u << k);
+                    }
+                };
+                const int dd = o2 - me.o;  // the other cell relative to mine
+                if constexpr (MERGE == kMergeCells) {
+                    if (dd == 0) {
+                        share(0, 0); share(1, 1); share(2, 2); share(3, 3);
+                    }
+                } else {
+                    if (me.wmd < 3 * MD) continue;
+                    if (dd == 0) {
+                        share(0, 0); share(1, 1); share(2, 2); share(3, 3);
+                    } else if (dd == MD) {                  // one pixel right
+                        share(1, 0); share(3, 2);
+                    } else if (dd == -MD) {                 // one pixel left
+                        share(0, 1); share(2, 3);
+                    } else if (dd == me.wmd) {              // one row down
+                        share(2, 0); share(3, 1);
+                    } else if (dd == -me.wmd) {             // one row up
+                        share(0, 2); share(1, 3);
+                    } else if (dd == me.wmd + MD) {         // down-right
+                        share(3, 0);
+                    } else if (dd == me.wmd - MD) {         // down-left
+                        share(2, 1);
+                    } else if (dd == MD - me.wmd) {         // up-right
+                        share(1, 2);
+                    } else if (dd == -MD - me.wmd) {        // up-left
+                        share(0, 3);
+                    }
                 }
-                if (same && jj > ln.c) smask = 0u;
             }
         }
 
@@ -1224,6 +1270,20 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
             }
         }
     }
+}
+
+template <typename T, typename ACC, int NV, bool FUSED, int MERGE>
+__global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
+    bwd4_body<T, ACC, NV, FUSED, MERGE>(a);
+}
+
+// The merging backward for one slot per lane, held to four resident blocks
+// per SM (64 registers): merging every corner would take it to 76 registers
+// and three blocks, and on GB300 the native encoder backward then keeps none
+// of the merge gains (344 us at three blocks, 306 us at four).
+template <typename T, typename ACC, bool FUSED, int MERGE>
+__global__ void __launch_bounds__(kBlockThreads, 4) msda_bwd4_merge1_kernel(const KernelArgs a) {
+    bwd4_body<T, ACC, 1, FUSED, MERGE>(a);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,10 @@
+// Kernel instantiations for bf16 I/O (see msda_device.cuh): the backward
+// into the fp32 workspace and its widen / convert kernels.
+#define MSDA_INSTANTIATE
+#include "msda_launch.cuh"
+
+namespace msda {
+template void launch_backward<__nv_bfloat16, float>(const KernelArgs&, const Plan&, cudaStream_t);
+template void launch_convert<__nv_bfloat16>(const float*, __nv_bfloat16*, long long, int, int, cudaStream_t);
+template void launch_widen<__nv_bfloat16>(const __nv_bfloat16*, float*, long long, int, cudaStream_t);
+}  // namespace msda

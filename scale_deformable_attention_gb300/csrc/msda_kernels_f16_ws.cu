@@ -1,0 +1,10 @@
+// Kernel instantiations for f16 I/O (see msda_device.cuh): the backward
+// into the fp32 workspace and its widen / convert kernels.
+#define MSDA_INSTANTIATE
+#include "msda_launch.cuh"
+
+namespace msda {
+template void launch_backward<__half, float>(const KernelArgs&, const Plan&, cudaStream_t);
+template void launch_convert<__half>(const float*, __half*, long long, int, int, cudaStream_t);
+template void launch_widen<__half>(const __half*, float*, long long, int, cudaStream_t);
+}  // namespace msda

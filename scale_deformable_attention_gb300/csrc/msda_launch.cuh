@@ -23,6 +23,7 @@ struct Plan {
     bool pdl;      // launched as a programmatic dependent of the kernel ahead of it
     int sms;       // multiprocessors of the device
     bool fused;    // fused operator (offsets + logits in, offset / logit gradients out)
+    bool merge;    // backward: merge the corners a point group's samples share before the scatter
 };
 
 #define MSDA_DISPATCH_NV(NVV, ...)                                   \
@@ -114,7 +115,19 @@ template <typename T, typename ACC, int NV, bool FUSED>
 static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     // with pl.pdl: may start while the zero kernel that precedes it still
     // runs; the kernel waits (griddepcontrol.wait) before its first scatter
-    launch_plan(msda_bwd4_kernel<T, ACC, NV, FUSED>, a, pl, st);
+    // merge mode: every shared corner for a 16-bit value into the fp32
+    // workspace, whole cells otherwise (the faster of the two on GB300 for
+    // each accumulator)
+    constexpr int MODE = (std::is_same<ACC, float>::value && sizeof(T) == 2) ? kMergeCorners : kMergeCells;
+    if (!pl.merge) {
+        launch_plan(msda_bwd4_kernel<T, ACC, NV, FUSED, 0>, a, pl, st);
+    } else {
+        // one slot per lane: the 64-register form (the integer accumulator's would spill)
+        if constexpr (NV == 1 && !std::is_same<ACC, long long>::value)
+            launch_plan(msda_bwd4_merge1_kernel<T, ACC, FUSED, MODE>, a, pl, st);
+        else
+            launch_plan(msda_bwd4_kernel<T, ACC, NV, FUSED, MODE>, a, pl, st);
+    }
 }
 
 template <typename T, typename ACC, int NV>

@@ -366,3 +366,33 @@ def test_stress_nine_batches_element_index_beyond_2_31():
     rows = np.unique(rng.choice(rows1, 2000, replace=False))
     got = f64(gv[B - 1].reshape(rows1, wl1.D)[torch.from_numpy(rows).to(DEV)])
     assert_grad("bf16", got, oracle.grad_value_rows(inp, "bf16", rows), "last batch grad_value (sampled rows)")
+
+
+@pytest.mark.parametrize("dtype,accum,tune_merge", [("f32", "auto", True), ("bf16", "native", True),
+                                                    ("bf16", "fp32", True), ("f16", "deterministic", True),
+                                                    ("f32", "deterministic", True), ("bf16", "native", False)])
+def test_clustered_samples_merge(dtype, accum, tune_merge):
+    """Each unit's points at a level lie within about a pixel of each other,
+    on levels 11, 3 and 1 pixels wide: the backward's corner merge sees
+    coinciding, edge- and corner-adjacent cells and chains of them (and skips
+    the narrow levels).  The inputs are dense (4*Q*L*K/S well above 2), so the
+    merge is on; the last case turns the density low so it is off."""
+    shapes = ((9, 11), (4, 3), (6, 1)) if tune_merge else ((60, 70), (40, 50), (30, 20))
+    wl = W.WORKLOADS["tiny_fp32"].with_(dtype=dtype, D=32 if dtype != "f32" else 16, B=2, Q=64 if tune_merge else 5,
+                                        M=3, K=4, shapes=shapes)
+    inp = dict(W.make_inputs(wl))
+    rng = np.random.default_rng(77)
+    L = len(shapes)
+    wh = np.array([[w, h] for h, w in shapes], dtype=np.float64)               # [L, 2] = (W, H)
+    centre = rng.uniform(0.0, 1.0, (wl.B, wl.Qn, wl.M, L, 1, 2))
+    loc = centre + rng.normal(0.0, 0.6, (wl.B, wl.Qn, wl.M, L, wl.K, 2)) / wh[None, None, None, :, None, :]
+    inp["sampling_locations"] = W.cast(loc, dtype).reshape(loc.shape)
+    msda = _msda()
+    assert (4.0 * wl.Qn * wl.L * wl.K / wl.S >= 2.0) == tune_merge
+    out, gv, gl, ga = _run(wl, inp, accum)
+    assert_forward(dtype, f64(out), oracle.forward(inp, dtype), "clustered out")
+    rgv, rgl, rga = oracle.backward(inp, dtype)
+    assert_grad(dtype, f64(gv), rgv, "clustered grad_value")
+    assert_grad(dtype, f64(gl), rgl, "clustered grad_loc")
+    assert_grad(dtype, f64(ga), rga, "clustered grad_attn")
+    assert msda.device_errors(clear=False) == 0
