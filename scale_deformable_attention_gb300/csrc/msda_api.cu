@@ -305,17 +305,16 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     pl.vec = vec;
     pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && NV <= 3 && !t.generic;
     pl.pdl = false;
-    pl.sms = sms;
     pl.fused = fused;
     a.ref = nullptr;
     a.gbuf_off = 0;
-    a.pdl_early = 0;
     // backward same-cell merge when samples are dense on the pyramid: on
     // average at least two corner contributions per pixel and head
     // (4*Q*L*K / S; measured: encoder 64 -> backward -19%, odd-D 2.6 -> -1.5%,
     // decoder 0.86 -> +10%)
     const double density = d.S > 0 ? 4.0 * (double)d.Q * (double)LK / (double)d.S : 0.0;
     pl.merge = t.merge >= 0 ? t.merge != 0 : density >= 2.0;
+    a.rbuf_off = -1;
     if (fused && backward) {
         const int64_t gbuf = (int64_t)tpb * LK * 4;
         int64_t off = mode != msda::PARAMS_DIRECT ? (int64_t)((pl.smem + 15) / 16 * 16) : 0;
@@ -325,6 +324,13 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
         }
         a.gbuf_off = (int)off;
         pl.smem = (size_t)(off + gbuf);
+        // grad_reference_points reduced in the kernel when a block holds
+        // whole queries and the per-sample grad_loc buffer fits
+        const int64_t rbuf = (int64_t)tpb * LK * 8, roff = (int64_t)((pl.smem + 15) / 16 * 16);
+        if (tpb % d.M == 0 && roff + rbuf <= 48 * 1024) {
+            a.rbuf_off = (int)roff;
+            pl.smem = (size_t)(roff + rbuf);
+        }
     }
     if (fused && !pl.spec)
         return fail(MSDA_ERR_UNSUPPORTED,
@@ -531,7 +537,10 @@ msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d
     a.grad_attn = grad_attn;
     a.err = di->err;
     a.det = hdr;
-    if (fz) a.ref = fz->ref;
+    if (fz) {
+        a.ref = fz->ref;
+        a.gref = fz->grad_ref;
+    }
     pl.pdl = pl.spec && !trace_active();
     {
         TraceScope ts(st);
@@ -565,7 +574,7 @@ msda_status backward_deterministic(msda_dtype dt, bool accumulate, const Dims& d
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
     }
-    if (fz) return launch_ref_grad(dt, d, shapes, grad_loc, fz->grad_ref, st);
+    if (fz && a.rbuf_off < 0) return launch_ref_grad(dt, d, shapes, grad_loc, fz->grad_ref, st);
     return MSDA_OK;
 }
 
@@ -834,7 +843,10 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
     a.grad_loc = grad_sampling_locations;
     a.grad_attn = grad_attention_weights;
     a.err = di->err;
-    if (fz) a.ref = fz->ref;
+    if (fz) {
+        a.ref = fz->ref;
+        a.gref = fz->grad_ref;
+    }
     pl.pdl = pl.spec && zeroed_here && !trace_active();
     {
         TraceScope ts(st);
@@ -867,7 +879,7 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
     }
-    if (fz) return launch_ref_grad(dt, d, spatial_shapes, grad_sampling_locations, fz->grad_ref, st);
+    if (fz && a.rbuf_off < 0) return launch_ref_grad(dt, d, spatial_shapes, grad_sampling_locations, fz->grad_ref, st);
     return MSDA_OK;
 }
 

@@ -96,7 +96,8 @@ struct KernelArgs {
     // grad_loc / grad_attn receive grad_offsets / grad_logits
     const void* ref;       // reference points [B, Q, L, 2]
     int gbuf_off;          // fused backward: byte offset of the per-sample <g, sampled> buffer in shared memory
-    int pdl_early;         // forward: let the next kernel launch at the start (whole grid resident)
+    int rbuf_off;          // fused backward: byte offset of the per-sample grad_loc buffer, or -1 (separate kernel)
+    void* gref;            // fused backward: grad_reference_points [B, Q, L, 2] (with rbuf_off >= 0)
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -791,13 +792,15 @@ __device__ __forceinline__ float dot2(const float (&g)[EPV], const float (&v)[EP
 
 // Samples whose corners a lane loads in one batch before using them.
 // Measured on GB300: in the forward, all four samples of a round for one
-// 16-byte slot per lane (encoder forward 122 -> 111 us), else two; in the
+// 16-byte slot per lane (encoder forward 122 -> 111 us), else two; the
+// fused forward keeps two (four: decoder 12.7 -> 16.1 us, encoder
+// 129 -> 150 us, its per-sample location and softmax work in between); in the
 // backward, two for every slot count: four slowed the encoder backward
 // (344 -> 367 us), and one halved the registers at three slots but slowed
 // the fp32 D=48 backward (211 -> 248 us).  Loads in flight per lane matter
 // more than occupancy here.
-template <int NV>
-constexpr int kGatherBatchFwd = NV == 1 ? 4 : 2;
+template <int NV, bool FUSED>
+constexpr int kGatherBatchFwd = (NV == 1 && !FUSED) ? 4 : 2;
 constexpr int kGatherBatchBwd = 2;
 
 // Channels [0, 4) and [16, 20) from p (16-bit elements, 8-byte aligned), as
@@ -851,7 +854,7 @@ __device__ __forceinline__ void fused_location(const KernelArgs& a, uint32_t bq,
 template <typename T, int NV, bool FUSED>
 __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelArgs a) {
     constexpr int EPV = 16 / sizeof(T);
-    constexpr int JB = kGatherBatchFwd<NV>;
+    constexpr int JB = kGatherBatchFwd<NV, FUSED>;
     using S_ = Slot<T, EPV>;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     __shared__ __align__(8) uint64_t bar;
@@ -861,14 +864,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
     // Launched as a programmatic dependent, this grid may start before the
     // kernel ahead of it (which may have written its inputs) has finished:
     // wait for it before reading anything.  Launched normally, the wait
-    // returns at once.  When the whole grid is resident (one wave), the next
-    // kernel may launch from the start and wait for this grid, which hides
-    // its launch.  With several waves it launches when this grid completes:
-    // its waiting blocks would take the SM slots of the later waves
-    // (measured on GB300: odd-D fp32 step +4% with a trigger at the end of
-    // each block, +15% with one at the start).
+    // returns at once.  The grid never lets the next kernel launch early:
+    // measured on GB300, an early trigger gained nothing for the core
+    // forward and cost the fused decoder step 13 us (its dependents' waiting
+    // blocks hold SM slots); the next kernel's own programmatic launch still
+    // overlaps this grid's completion.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (a.pdl_early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Lane ln = lane_of(a);
     if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
         if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
@@ -1125,6 +1126,11 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
                 gl[2 * ps + 1] = Elem<T>::from_f(wa * ry);
                 gbuf[s_own] = ra;
                 pdot += wa * ra;
+                if (a.rbuf_off >= 0) {  // grad_loc, summed into grad_reference_points below
+                    float* rb = reinterpret_cast<float*>(sm + a.rbuf_off) + ((long long)ln.team * a.LK + s_own) * 2;
+                    rb[0] = wa * rx * lev.fW;
+                    rb[1] = wa * ry * lev.fH;
+                }
             } else {
                 ga[ps] = Elem<T>::from_f(ra);
                 gl[2 * ps] = Elem<T>::from_f(wa * lev.fW * rx);
@@ -1231,28 +1237,26 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
                 const float2 cf = make_float2(cj[k], cj[k]);
 #pragma unroll
                 for (int n = 0; n < NV; ++n) {
-                    float t[EPV];
+                    if constexpr (ILV) {
+                        // each contribution times 2^F (exact), rounded once to an integer
+                        long long* q = ibase + off[k] + n * kC * EPV;
 #pragma unroll
-                    for (int e = 0; e < EPV; e += 2) {
-                        const float2 r = __fmul2_rn(cf, make_float2(g[n][e], g[n][e + 1]));
-                        t[e] = r.x;
-                        t[e + 1] = r.y;
-                    }
-                    if constexpr (std::is_same<ACC, long long>::value) {
-                        if constexpr (ILV) {
-                            long long* q = ibase + off[k] + n * kC * EPV;
-#pragma unroll
-                            for (int e = 0; e < EPV; ++e)
-                                red_s64(q + kC * e, __float2ll_rn(cf.x * gi[n][e] * dscale));
-                        } else {
-                            det_scatter<EPV>(gbase + off[k] + n * kC * EPV, t, dscale);
-                        }
-                    } else if constexpr (SPLIT) {
-                        float* q = gbase + off[k] + n * kC * EPV;
-                        red_v4_f32(q, t[0], t[1], t[2], t[3]);
-                        red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+                        for (int e = 0; e < EPV; ++e) red_s64(q + kC * e, __float2ll_rn(cf.x * gi[n][e] * dscale));
                     } else {
-                        Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                        float t[EPV];
+#pragma unroll
+                        for (int e = 0; e < EPV; e += 2) {
+                            const float2 r = __fmul2_rn(cf, make_float2(g[n][e], g[n][e + 1]));
+                            t[e] = r.x;
+                            t[e + 1] = r.y;
+                        }
+                        if constexpr (SPLIT) {
+                            float* q = gbase + off[k] + n * kC * EPV;
+                            red_v4_f32(q, t[0], t[1], t[2], t[3]);
+                            red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+                        } else {
+                            Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                        }
                     }
                 }
             }
@@ -1267,6 +1271,24 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
             if (ln.active && s_own < a.LK) {
                 const float A = expf(read_weight<T>(a, sm, staged, ln.team, ln.u, s_own) - smx) / ssum;
                 ga[(long long)ln.u * a.LK + s_own] = Elem<T>::from_f(A * (gbuf[s_own] - pdot));
+            }
+        }
+        // grad_reference_points[b, q, l] = sum over (m, k) of grad_loc, when
+        // the block holds whole queries (units per block a multiple of M):
+        // one thread per output, a fixed summation order
+        if (a.rbuf_off >= 0) {
+            __syncthreads();
+            const float* rb = reinterpret_cast<const float*>(sm + a.rbuf_off);
+            const int nq = min(a.tpb, a.n_units - (int)ln.u0) / a.M;
+            for (int t = threadIdx.x; t < nq * a.L * 2; t += blockDim.x) {
+                const int c = t & 1, l = (t >> 1) % a.L, ql = (t >> 1) / a.L;
+                float acc = 0.f;
+                for (int m = 0; m < a.M; ++m) {
+                    const float* r = rb + ((ql * a.M + m) * a.LK + l * a.K) * 2 + c;
+                    for (int k = 0; k < a.K; ++k) acc += r[2 * k];
+                }
+                const long long bq = (long long)(ln.u0 / (uint32_t)a.M) + ql;
+                reinterpret_cast<T*>(a.gref)[(bq * a.L + l) * 2 + c] = Elem<T>::from_f(acc);
             }
         }
     }

@@ -4,8 +4,6 @@
 // translation unit (msda_kernels_<dtype>.cu) so they compile in parallel.
 #pragma once
 
-#include <mutex>
-
 #include "msda_device.cuh"
 
 namespace msda {
@@ -21,7 +19,6 @@ struct Plan {
     bool wide;     // 64-bit offsets inside a batch slice
     bool spec;     // specialised kernels: C = 4, nvec == 4 * nv, nv <= 3, 32-bit offsets
     bool pdl;      // launched as a programmatic dependent of the kernel ahead of it
-    int sms;       // multiprocessors of the device
     bool fused;    // fused operator (offsets + logits in, offset / logit gradients out)
     bool merge;    // backward: merge the corners a point group's samples share before the scatter
 };
@@ -73,42 +70,11 @@ static inline void launch_plan(void (*kernel)(const KernelArgs), const KernelArg
     }
 }
 
-// Whether all of `kernel`'s grid is resident at once (one wave), by the
-// occupancy calculator; cached per kernel and shared-memory size.
-static inline bool one_wave(void (*kernel)(const KernelArgs), const Plan& pl) {
-    struct Entry {
-        const void* k;
-        size_t smem;
-        int blocks;
-    };
-    static Entry cache[64];
-    static int n = 0;
-    static std::mutex mu;
-    int per_sm = -1;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        for (int i = 0; i < n; ++i)
-            if (cache[i].k == (const void*)kernel && cache[i].smem == pl.smem) per_sm = cache[i].blocks;
-    }
-    if (per_sm < 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (int)(pl.block.x * pl.block.y), pl.smem) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            per_sm = 0;
-        }
-        std::lock_guard<std::mutex> lk(mu);
-        if (n < 64) cache[n++] = Entry{(const void*)kernel, pl.smem, per_sm};
-    }
-    return (long long)pl.grid.x * pl.grid.y <= (long long)per_sm * pl.sms;
-}
-
 template <typename T, int NV>
 static void fwd4_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     // the kernel waits for the kernel ahead of it before reading anything
-    void (*k)(const KernelArgs) = pl.fused ? msda_fwd4_kernel<T, NV, true> : msda_fwd4_kernel<T, NV, false>;
-    KernelArgs b = a;
-    b.pdl_early = pl.pdl && one_wave(k, pl) ? 1 : 0;
-    launch_plan(k, b, pl, st);
+    if (pl.fused) launch_plan(msda_fwd4_kernel<T, NV, true>, a, pl, st);
+    else launch_plan(msda_fwd4_kernel<T, NV, false>, a, pl, st);
 }
 
 template <typename T, typename ACC, int NV, bool FUSED>
