@@ -683,10 +683,12 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = units * args.steps / el
     sample = f"first {q} of {wl.Qn} queries of every batch ({units} units) per step"
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": 0,
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "Q": wl.Qn, "M": wl.M, "D": wl.D, "L": wl.L, "K": wl.K},
+            "config": {"workload": wl.name, "B": wl.B, "Q": wl.Qn, "M": wl.M, "D": wl.D, "L": wl.L, "K": wl.K,
+                       "S": wl.S, "spatial_shapes": [list(x) for x in wl.shapes], "accum": "fp64 (oracle)",
+                       "parallelism": f"host cores ({oracle.num_threads()} threads), rank 0 only"},
             "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
