@@ -325,6 +325,35 @@ def unique_fractions(model: dict, kernels: dict, peak: float):
             "peak": peak, "unit": "GB/s"}
 
 
+def reduction_ceiling_for(accum: str, dtype: str):
+    """32-byte reduction sectors per second the L2 takes for this backward's
+    kind of reduction (msda_reduction_ceiling), or None (the deterministic
+    accumulator's scalar integer reductions are another pattern)."""
+    import torch
+
+    import scale_deformable_attention_gb300 as msda
+
+    if accum == "deterministic":
+        return None
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+    return msda.reduction_ceiling(tdt if accum == "native" else torch.float32)
+
+
+def reduction_roofline(wl: W.Workload, corners: int, accum: str, kernels: dict, ceiling):
+    """The backward kernel against the L2's reduction ceiling: algorithmic
+    sectors = in-level corner rows x 32-byte sectors per row at the
+    accumulator's width (before the corner merge), over the traced kernel time."""
+    if not ceiling or "backward" not in kernels:
+        return None
+    es_acc = W.ESIZE[wl.dtype] if accum == "native" else 4
+    sectors = corners * ((wl.D * es_acc + 31) // 32)
+    achieved = sectors / (kernels["backward"]["avg_ms"] / 1e3)
+    return {"kernel": "backward", "bound": "l2_reductions", "sectors": sectors,
+            "achieved_gsectors_s": round(achieved / 1e9, 2), "ceiling_gsectors_s": round(ceiling / 1e9, 2),
+            "frac": round(achieved / ceiling, 4),
+            "ceiling_source": "msda_reduction_ceiling on this GPU (random sectors, two 16-byte reductions each)"}
+
+
 def run_ours(args):
     import torch
 
@@ -342,6 +371,7 @@ def run_ours(args):
     st = GpuStep(wl, inp, accum, device)
     corners, urows = corner_counts(wl, inp)
     model = byte_model(wl, corners, urows)
+    red_ceiling = reduction_ceiling_for(st.resolved, wl.dtype)
 
     for _ in range(max(args.warmup, 3)):
         st.flush()
@@ -402,6 +432,7 @@ def run_ours(args):
             "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
             "roofline": roof, "kernels": kernels, "bytes_per_step_model": model["step"],
             "unique_model": unique_fractions(model, kernels, peak),
+            "reduction_roofline": reduction_roofline(wl, corners, st.resolved, kernels, red_ceiling),
             "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
             "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "traced_steps_every": args.trace_every,
         }

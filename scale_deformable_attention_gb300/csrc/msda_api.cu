@@ -473,6 +473,7 @@ msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
 
 namespace msda {
 msda_status set_error(msda_status s, const char* message) { return fail(s, "%s", message); }
+void clear_error() { g_msg[0] = 0; }
 }  // namespace msda
 
 namespace {
