@@ -123,7 +123,11 @@ struct TraceScope {
     }
 };
 
-// ---- tuning overrides (sweeps only): MSDA_TUNE="C=4,P=2,params=bulk|ld|direct" ----
+// ---- tuning overrides (sweeps and tests), read once per process ----
+// MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
+// params=bulk|ld|direct, generic, notma, tma, pointparallel, nopdl, merge,
+// nomerge.  None of them changes results beyond the rounding order of the
+// grad_value sums.
 
 struct Tune {
     int C = 0, P = 0, params = -1;
@@ -132,7 +136,7 @@ struct Tune {
     bool tma = false;      // TMA-gather forward whatever the size
     bool pointparallel = false;  // the point-parallel ablation forward (D = 32 only)
     bool pdl = true;       // forward and zero kernel as programmatic dependents (off: nopdl)
-    int merge = -1;        // backward same-cell merge: -1 by density, 0 off (nomerge), 1 on (merge)
+    int merge = -1;        // backward corner merge: -1 by density, 0 off (nomerge), 1 on (merge)
 };
 const Tune& tune() {
     static Tune t = [] {
