@@ -1,0 +1,70 @@
+"""The algorithmic byte models bench.py reports rooflines with, checked on
+small workloads against a plain loop over samples and corners: the number of
+in-level (sample, corner) pairs (per-corner model) and of distinct value rows
+(unique model), on the binary32 pixel coordinate the kernels use."""
+import importlib.util
+import math
+import os
+import sys
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    argv, sys.argv = sys.argv, ["bench.py"]
+    try:
+        spec.loader.exec_module(mod)
+    finally:
+        sys.argv = argv
+    return mod
+
+
+def loop_counts(wl, inp):
+    loc = W.to_f64(inp["sampling_locations"], wl.dtype)
+    starts = W.level_start_index(wl.shapes)
+    B, Q, M = loc.shape[:3]
+    n, rows = 0, set()
+    for b in range(B):
+        for q in range(Q):
+            for m in range(M):
+                for l, (h, w) in enumerate(wl.shapes):
+                    for k in range(wl.K):
+                        x = math.floor(float(np.float32(loc[b, q, m, l, k, 0] * w - 0.5)))
+                        y = math.floor(float(np.float32(loc[b, q, m, l, k, 1] * h - 0.5)))
+                        for dy in (0, 1):
+                            for dx in (0, 1):
+                                if 0 <= x + dx < w and 0 <= y + dy < h:
+                                    n += 1
+                                    rows.add(((b * wl.S + starts[l] + (y + dy) * w + x + dx) * M + m))
+    return n, len(rows)
+
+
+@pytest.mark.parametrize("name,over", [("tiny_fp32", {}), ("tiny_fp32", {"dtype": "bf16", "B": 2, "Q": 33, "M": 3}),
+                                       ("decoder_bf16", {"B": 1, "Q": 7})])
+def test_corner_counts_match_a_loop(bench, name, over):
+    wl = W.WORKLOADS[name].with_(**over) if over else W.WORKLOADS[name]
+    inp = W.make_inputs(wl)
+    assert bench.corner_counts(wl, inp) == loop_counts(wl, inp)
+
+
+def test_byte_model_formula(bench):
+    wl = W.WORKLOADS["decoder_bf16"]
+    es = 2
+    corners, rows = 596431, 265129
+    m = bench.byte_model(wl, corners, rows)
+    samples = wl.B * wl.Qn * wl.M * wl.L * wl.K
+    out = wl.B * wl.Qn * wl.M * wl.D * es
+    n_value = wl.B * wl.S * wl.M * wl.D
+    assert m["forward"] == corners * wl.D * es + samples * 3 * es + out
+    assert m["backward"] == 2 * corners * wl.D * es + out + 2 * samples * 3 * es
+    assert m["bwd_total"] == m["backward"] + n_value * es
+    assert m["forward_unique"] == rows * wl.D * es + samples * 3 * es + out
+    assert m["bwd_total_unique"] == rows * wl.D * es + out + 2 * samples * 3 * es + n_value * es
