@@ -105,3 +105,37 @@ def test_backward_inputs_from_the_kernel_ahead():
         for got, ref, what in zip((gv, gl, ga), want, ("grad_value", "grad_loc", "grad_attn")):
             assert_grad(wl.dtype, f64(got), ref, what)
     assert np.isfinite(f64(big[:4])).all()
+
+
+def test_two_streams_run_independent_problems():
+    """Two problems on two streams at once (programmatic launches on both):
+    each matches the oracle, whatever the interleaving."""
+    import scale_deformable_attention_gb300 as msda
+
+    cases = []
+    for seed, name in ((5, "decoder_bf16"), (6, "oddD_fp32")):
+        wl = W.WORKLOADS[name].with_(B=2, seed=seed)
+        inp = W.make_inputs(wl)
+        cases.append((wl, inp, to_torch(inp, wl.dtype, DEV), torch.cuda.Stream()))
+    torch.cuda.synchronize()
+    results = []
+    for _ in range(3):
+        outs = []
+        for wl, inp, t, s in cases:
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                out = msda.forward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                                   t["attention_weights"], validate=False)
+                grads = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"],
+                                      t["sampling_locations"], t["attention_weights"], t["grad_out"], validate=False)
+            outs.append((out, grads))
+        torch.cuda.synchronize()
+        results.append(outs)
+    for (wl, inp, _, _), k in zip(cases, range(2)):
+        want_out = oracle.forward(inp, wl.dtype)
+        want = oracle.backward(inp, wl.dtype)
+        for outs in results:
+            out, (gv, gl, ga) = outs[k]
+            assert_forward(wl.dtype, f64(out), want_out, f"{wl.name} out")
+            for got, ref, what in zip((gv, gl, ga), want, ("grad_value", "grad_loc", "grad_attn")):
+                assert_grad(wl.dtype, f64(got), ref, f"{wl.name} {what}")
