@@ -125,8 +125,8 @@ struct TraceScope {
 
 // ---- tuning overrides (sweeps and tests), read once per process ----
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
-// params=bulk|ld|direct, generic, notma, tma, pointparallel, nopdl, merge,
-// nomerge.  None of them changes results beyond the rounding order of the
+// params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
+// merge, nomerge.  None of them changes results beyond the rounding order of the
 // grad_value sums.
 
 struct Tune {
@@ -136,6 +136,7 @@ struct Tune {
     bool tma = false;      // TMA-gather forward whatever the size
     bool pointparallel = false;  // the point-parallel ablation forward (D = 32 only)
     bool pdl = true;       // forward and zero kernel as programmatic dependents (off: nopdl)
+    bool spec = false;     // the specialised forward even where the generic one is faster
     int merge = -1;        // backward corner merge: -1 by density, 0 off (nomerge), 1 on (merge)
 };
 const Tune& tune() {
@@ -156,6 +157,7 @@ const Tune& tune() {
             else if (!strcmp(tok, "tma")) r.tma = true;
             else if (!strcmp(tok, "pointparallel")) r.pointparallel = true;
             else if (!strcmp(tok, "nopdl")) r.pdl = false;
+            else if (!strcmp(tok, "spec")) r.spec = true;
             else if (!strcmp(tok, "merge")) r.merge = 1;
             else if (!strcmp(tok, "nomerge")) r.merge = 0;
         }
@@ -635,6 +637,17 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
     KernelArgs a{};
     Plan pl{};
     if ((s = make_plan(dt, d, vec, di->sms, false, loc, attn, pl, a, ref != nullptr, big ? 2 : 1))) return s;
+    // One 16-bit slot per lane and few samples (at most 2^20): the generic
+    // forward, whose lanes each set up their own samples, is faster than the
+    // specialised one, whose setup-then-shuffle chain lengthens a latency-bound
+    // wave.  Measured on GB300, bf16 D=32 decoder: B=1 10.3 -> 8.2 us,
+    // B=4 14.2 -> 12.3 us, B=16 31.5 -> 28.7 us.  With many samples the forward
+    // is issue-bound and the redundant setups cost more (encoder 111 -> 131 us);
+    // with two slots or more the specialised one stays ahead (D=64 bf16 or
+    // D=32 fp32: +3-4% generic).
+    const int64_t samples = d.units * d.L * d.K;
+    if (!ref && pl.spec && pl.nv == 1 && es == 2 && samples <= (1ll << 20) && !tune().spec && !tune().tma)
+        pl.spec = false;
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;
@@ -677,7 +690,7 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
         default: msda::launch_forward_tma<__nv_bfloat16>(a, map, pl.nv, grid, st); break;
         }
     } else {
-        pl.pdl = pl.spec && tune().pdl && !trace_active();
+        pl.pdl = tune().pdl && !trace_active();
         switch (dt) {
         case MSDA_F32: msda::launch_forward<float>(a, pl, st); break;
         case MSDA_F16: msda::launch_forward<__half>(a, pl, st); break;

@@ -504,6 +504,10 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd_kernel(const KernelArg
     __shared__ int verdict;
     extern __shared__ __align__(16) unsigned char sm[];
 
+    // launched as a programmatic dependent: wait for the kernel ahead of it
+    // (which may have written its inputs) before reading anything; launched
+    // normally, the wait returns at once
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Lane ln = lane_of(a);
     if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
         if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);

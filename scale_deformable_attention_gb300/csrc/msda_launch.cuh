@@ -31,11 +31,6 @@ struct Plan {
     default: { constexpr int NV = 4; __VA_ARGS__; } break;           \
     }
 
-template <typename T, int NV, int EPV, bool WIDE>
-static void fwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
-    msda_fwd_kernel<T, NV, EPV, WIDE, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
-}
-
 template <typename T, typename ACC, int NV, int EPV, bool WIDE>
 static void bwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     msda_bwd_kernel<T, ACC, NV, EPV, WIDE, kSamplesInFlight><<<pl.grid, pl.block, pl.smem, st>>>(a);
@@ -68,6 +63,12 @@ static inline void launch_plan(void (*kernel)(const KernelArgs), const KernelArg
     } else {
         kernel<<<pl.grid, pl.block, pl.smem, st>>>(a);
     }
+}
+
+template <typename T, int NV, int EPV, bool WIDE>
+static void fwd_go(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    // the kernel waits for the kernel ahead of it before reading anything
+    launch_plan(msda_fwd_kernel<T, NV, EPV, WIDE, kSamplesInFlight>, a, pl, st);
 }
 
 template <typename T, int NV>

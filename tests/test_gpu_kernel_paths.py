@@ -1,7 +1,8 @@
 """Every kernel family against the oracle, whatever the size heuristics pick:
-the TMA-gather forward, the generic kernels, direct (unstaged) parameter
-loads, the staged loads without the bulk copy, the backward's same-cell merge
-forced on and off, and ordinary (non-programmatic) launches.  Each runs in a
+the TMA-gather forward, the generic kernels, the specialised forward where
+the generic one is chosen (small one-slot 16-bit problems), direct (unstaged)
+parameter loads, the staged loads without the bulk copy, the backward's
+corner merge forced on and off, and ordinary (non-programmatic) launches.  Each runs in a
 child process with MSDA_TUNE set."""
 import os
 import subprocess
@@ -14,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel",
-                                  "merge", "nomerge", "nopdl", "merge,P=2"])
+                                  "merge", "nomerge", "nopdl", "merge,P=2", "spec"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
