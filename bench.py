@@ -354,6 +354,29 @@ def reduction_roofline(wl: W.Workload, corners: int, accum: str, kernels: dict, 
             "ceiling_source": "msda_reduction_ceiling on this GPU (random sectors, two 16-byte reductions each)"}
 
 
+def graph_cross_check(st, steps: int):
+    """The step captured once as a CUDA graph and replayed, timed like the
+    bench's steps (L2 flushed, then events around each replay), beside the
+    same number of stream-launched steps: a cross-check of the step time."""
+    torch = st.torch
+    s = torch.cuda.Stream(st.device)
+    s.wait_stream(torch.cuda.current_stream(st.device))
+    with torch.cuda.stream(s):
+        st.step()
+    torch.cuda.current_stream(st.device).wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.step()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    replay = st.timed(g.replay, steps)
+    stream = st.timed(st.step, steps)
+    del g
+    return {"steps": steps, "graph_ms_per_step": round(sum(replay) / steps, 5),
+            "stream_ms_per_step": round(sum(stream) / steps, 5)}
+
+
 def run_ours(args):
     import torch
 
@@ -383,14 +406,18 @@ def run_ours(args):
     recs, _ = msda.trace_read()
     launches_per_step = len(recs)
 
-    msda.trace_enable(4 * (args.steps // args.trace_every + 2))
+    # trace one step in 64 (at least 8 traced steps): a traced step runs its
+    # kernels without programmatic launches and with events between them, so
+    # each costs the headline time it is part of
+    trace_every = args.trace_every if args.trace_every > 0 else max(1, min(64, args.steps // 8))
+    msda.trace_enable(4 * (args.steps // trace_every + 2))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     with ClockSampler(uuid) as clk:
-        times = st.timed(st.step, args.steps, trace_every=args.trace_every)
+        times = st.timed(st.step, args.steps, trace_every=trace_every)
     torch.cuda.synchronize()
     recs, dropped = msda.trace_read()
     msda.trace_enable(0)
@@ -416,6 +443,7 @@ def run_ours(args):
     kernels = {k: {"launches": len(v), "avg_ms": round(statistics.mean(v), 5),
                    "share": round(sum(v) / sum(sum(x) for x in per.values()), 4)} for k, v in per.items()}
 
+    graph = graph_cross_check(st, min(args.steps, 2000)) if not args.no_graph else None
     e2e = run_e2e(st, inp, args) if not args.no_e2e else None
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -434,7 +462,8 @@ def run_ours(args):
             "unique_model": unique_fractions(model, kernels, peak),
             "reduction_roofline": reduction_roofline(wl, corners, st.resolved, kernels, red_ceiling),
             "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
-            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "traced_steps_every": args.trace_every,
+            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "traced_steps_every": trace_every,
+            "graph_cross_check": graph,
         }
         print(json.dumps(line), flush=True)
     if args.all and rank == 0:
@@ -740,10 +769,11 @@ def main(argv=None):
     ap.add_argument("--fused", action="store_true",
                     help="also print fused-operator vs PyTorch-ops-around-the-core tables")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay cross-check")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--trace-every", type=int, default=16,
-                    help="record per-kernel events on every n-th timed step")
+    ap.add_argument("--trace-every", type=int, default=0,
+                    help="record per-kernel events on every n-th timed step (0: one in 64, at least 8 steps)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
     args = ap.parse_args(argv)
