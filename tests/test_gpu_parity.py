@@ -237,12 +237,16 @@ def test_forward_is_deterministic():
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("dtype,accum", [("f32", "auto"), ("bf16", "fp32"), ("f16", "native")])
-def test_accumulate_doubles(dtype, accum):
+@pytest.mark.parametrize("dtype,accum,dense", [("f32", "auto", False), ("bf16", "fp32", False), ("f16", "native", False),
+                                               ("bf16", "fp32", True), ("f16", "native", True)])
+def test_accumulate_doubles(dtype, accum, dense):
     """Backward into the previous call's grad_value adds the same gradient again
-    (up to summation order)."""
+    (up to summation order).  Dense cases (many samples per pixel) run with the
+    backward's corner merge on."""
     msda = _msda()
-    wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, B=1, Q=120)
+    over = dict(shapes=((20, 24), (10, 12), (5, 6), (3, 3))) if dense else {}
+    wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, B=1, Q=120, **over)
+    assert (4.0 * wl.Qn * wl.L * wl.K / wl.S >= 2.0) == dense
     inp = W.make_inputs(wl)
     t = to_torch(inp, dtype, DEV)
     args = (t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"], t["attention_weights"],
