@@ -122,6 +122,8 @@ typedef enum {
  * every non-empty tensor pointer non-NULL and aligned to its element size.
  * Rows of 16-byte multiples with 16-byte aligned value/out take the vector
  * path; anything else takes the element-wise path, with identical results.
+ * The kernel may be launched as a programmatic dependent of the work ahead of
+ * it on `stream`; it waits for that work before reading anything.
  */
 msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K,
                          int64_t Q, const void* value, const int64_t* spatial_shapes,
@@ -155,7 +157,14 @@ msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t
  * grad_value is zeroed on `stream` first, unless `flags` has
  * MSDA_BWD_ACCUMULATE, in which case the gradient is added to its contents.
  * grad_value is summed by relaxed atomic adds, so its bits may differ between
- * runs (course ch. 5, "Atomics make gradients nondeterministic").
+ * runs (course ch. 5, "Atomics make gradients nondeterministic"), except with
+ * MSDA_ACCUM_DETERMINISTIC.  When samples are dense on the pyramid, the
+ * coefficients of a unit's samples that share corner rows are added before
+ * the reduction: this changes only the order of the additions.
+ *
+ * Like msda_forward, the kernels may be launched as programmatic dependents
+ * of the work ahead of them on `stream`; each waits for that work before
+ * reading or writing memory, so stream order holds for the caller.
  *
  * `workspace` (device, 16-byte aligned, >= msda_backward_workspace_size()
  * bytes) is used only by the FP32 and DETERMINISTIC accumulators and may be
