@@ -14,7 +14,12 @@ Entry points:
   sampling_locations, attention_weights, fp32_grad_accum=None)`` -- the
   differentiable operator (signature of the README's quickstart);
 * ``forward(...)`` / ``backward(...)`` -- the two C-ABI calls;
-* ``device_errors()``, ``trace_enable()`` / ``trace_read()`` -- diagnostics.
+* ``multi_scale_deformable_attention_fused(...)``, ``forward_fused(...)`` /
+  ``backward_fused(...)`` -- the fused operator (softmax of the attention
+  logits and reference point + offset / (W, H) inside the kernels);
+* ``device_errors()``, ``trace_enable()`` / ``trace_read()`` -- diagnostics;
+* ``reduction_ceiling()`` -- the L2's rate for the backward's reduction
+  traffic, for roofline reporting.
 """
 from __future__ import annotations
 
@@ -110,7 +115,7 @@ def forward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_index
 
 
 def resolve_accum(dtype: torch.dtype, accum: str, dims) -> str:
-    """Which grad_value accumulator ("native" or "fp32") the backward uses."""
+    """Which grad_value accumulator ("native", "fp32" or "deterministic") the backward uses."""
     r = _lib.lib().msda_resolve_accum(DTYPE_CODE[dtype], ACCUM[accum], *dims)
     return _lib.ACCUM_NAMES[r]
 
