@@ -46,7 +46,8 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 # ---------------------------------------------------------------------------
-# byte model (algorithmic bytes per launch)
+# byte models (algorithmic bytes per launch): per-corner (every in-level
+# corner row counted each time) and unique (each distinct value row once)
 
 def corner_counts(wl: W.Workload, inp, unique: bool = True):
     """(in-bounds (sample, corner) pairs, distinct value rows they touch), on
