@@ -169,3 +169,12 @@ def test_fused_rejects_rows_it_cannot_vectorise(dtype, D):
         msda.forward_fused(*_args(t))
     with pytest.raises(msda._lib.MsdaError, match="fused operator"):
         msda.backward_fused(*_args(t), t["grad_out"])
+
+
+@pytest.mark.parametrize("M", [1, 16, 32])
+def test_fused_head_counts(M):
+    """grad_reference_points is reduced inside the backward when a block holds
+    whole queries (units per block a multiple of M), else by a separate
+    kernel: single head, many heads, and more heads than a block's units."""
+    wl = W.WORKLOADS["decoder_bf16"].with_(B=2, Q=37, M=M, shapes=((30, 40), (15, 20), (8, 10), (4, 5)))
+    _check(wl, W.make_fused_inputs(wl), "auto", f"M={M}")
