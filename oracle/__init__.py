@@ -67,6 +67,8 @@ def _load(path: str):
               "msda_oracle_backward_units", "msda_oracle_grad_value_rows"):
         getattr(lib, f).restype = ip
     lib.msda_oracle_num_threads.restype = ip
+    lib.msda_oracle_fused_locations.argtypes = [ip] + [i64] * 5 + [vp, vp, vp, vp]
+    lib.msda_oracle_fused_locations.restype = ip
     return lib
 
 
@@ -188,11 +190,27 @@ def grad_value_rows(inp, dtype: str, rows: np.ndarray, coord_mode: int = 1, nthr
 # point mapped to level l plus the learned offset.  Reading taken: offsets are
 # in pixels of level l, so loc = ref + offset / (W_l, H_l) (x by W, y by H).
 
+def fused_locations(ref: np.ndarray, off: np.ndarray, shapes: np.ndarray, coord_mode: int = 1) -> np.ndarray:
+    """Sampling locations [B,Q,M,L,K,2] of the fused operator from fp64 reference
+    points [B,Q,L,2] and pixel offsets [B,Q,M,L,K,2] (C oracle):
+    loc = ref + off / (W_l, H_l), in binary32 with one rounding per operation
+    (coord_mode 1, as the kernels) or in fp64 (coord_mode 0)."""
+    ref = np.ascontiguousarray(ref, dtype=np.float64)
+    off = np.ascontiguousarray(off, dtype=np.float64)
+    shapes = np.ascontiguousarray(shapes, dtype=np.int64)
+    B, Q, M, L, K, _ = off.shape
+    if ref.shape != (B, Q, L, 2) or shapes.shape != (L, 2):
+        raise ValueError("fused_locations: reference points must be [B,Q,L,2] and shapes [L,2]")
+    loc = np.zeros(off.shape, dtype=np.float64)
+    _check(_lib().msda_oracle_fused_locations(int(coord_mode), B, Q, M, L, K, _ptr(shapes), _ptr(ref), _ptr(off),
+                                              _ptr(loc)), "fused_locations")
+    return loc
+
+
 def fused_core_inputs(inp, dtype: str, coord_mode: int = 1):
     """(core inputs with fp64 loc / attn, A [B,Q,M,L,K], normaliser [L,2]) of a
-    fused problem.  coord_mode 1 computes loc = ref + off / W in binary32 (one
-    rounding per operation, as the kernel does) so the cell decision matches;
-    coord_mode 0 in fp64.  A is the fp64 softmax."""
+    fused problem.  The locations come from ``fused_locations`` (binary32 in
+    coord_mode 1, fp64 in coord_mode 0); A is the fp64 softmax."""
     from workloads import to_f64
 
     ref = to_f64(inp["reference_points"], dtype)        # [B,Q,L,2]
@@ -201,12 +219,7 @@ def fused_core_inputs(inp, dtype: str, coord_mode: int = 1):
     shapes = np.asarray(inp["spatial_shapes"], dtype=np.int64)
     B, Q, M, L, K, _ = off.shape
     norm = np.stack([shapes[:, 1], shapes[:, 0]], axis=-1).astype(np.float64)   # [L,2] = (W, H)
-    refb = ref[:, :, None, :, None, :]
-    nb = norm[None, None, None, :, None, :]
-    if coord_mode == 1:
-        loc = (refb.astype(np.float32) + off.astype(np.float32) / nb.astype(np.float32)).astype(np.float64)
-    else:
-        loc = refb + off / nb
+    loc = fused_locations(ref, off, shapes, coord_mode)
     z = logits - logits.max(axis=-1, keepdims=True)
     e = np.exp(z)
     A = (e / e.sum(axis=-1, keepdims=True)).reshape(B, Q, M, L, K)

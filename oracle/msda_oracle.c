@@ -369,3 +369,45 @@ int msda_oracle_grad_value_rows(PROB_ARGS, const void* grad_out, const int64_t* 
             }
     return 0;
 }
+
+/* ---- fused operator: sampling locations from reference points and offsets ----
+ *
+ * msda-triton README, "The operator": the sampling location is the reference
+ * point mapped to level l plus the learned offset.  Reading taken: the
+ * reference point [B,Q,L,2] is normalised to [0,1] and shared by all levels,
+ * the offset [B,Q,M,L,K,2] is in pixels of level l, so
+ *
+ *   loc.x = ref.x + off.x / W_l,   loc.y = ref.y + off.y / H_l.
+ *
+ * coord_mode 1 takes each operation in binary32 with one rounding (the
+ * quotient, then the sum), as the kernels do, so that the cell decision made
+ * on the result matches theirs; coord_mode 0 takes them in fp64.  Inputs and
+ * the output are fp64 (the inputs hold exactly representable binary32,
+ * binary16 or bfloat16 values). */
+int msda_oracle_fused_locations(int coord_mode, int64_t B, int64_t Q, int64_t M, int64_t L, int64_t K,
+                                const int64_t* shapes, const double* ref, const double* off, double* loc) {
+    if (B < 0 || Q < 0 || M < 0 || L < 1 || K < 1 || (coord_mode != 0 && coord_mode != 1)) return 1;
+    for (int64_t l = 0; l < L; ++l)
+        if (shapes[2 * l] < 1 || shapes[2 * l + 1] < 1) return 2;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t q = 0; q < Q; ++q)
+            for (int64_t m = 0; m < M; ++m)
+                for (int64_t l = 0; l < L; ++l) {
+                    const double* r = ref + ((b * Q + q) * L + l) * 2;
+                    double size[2] = {(double)shapes[2 * l + 1], (double)shapes[2 * l]};   /* (W, H) */
+                    for (int64_t k = 0; k < K; ++k) {
+                        int64_t p = (((b * Q + q) * M + m) * L + l) * K + k;
+                        for (int c = 0; c < 2; ++c) {
+                            double o = off[2 * p + c];
+                            if (coord_mode == 1) {
+                                float quot = (float)o / (float)size[c];
+                                float sum = (float)r[c] + quot;
+                                loc[2 * p + c] = (double)sum;
+                            } else {
+                                loc[2 * p + c] = r[c] + o / size[c];
+                            }
+                        }
+                    }
+                }
+    return 0;
+}

@@ -535,9 +535,61 @@ def pin_fused_finite_differences():
         _close(grad.reshape(-1), fd, 1e-6, atol=1e-8, what=f"fused finite differences {key}")
 
 
+def pin_fused_coordinate_modes_agree():
+    """The fused locations in binary32 (coord_mode 1, the kernels' arithmetic)
+    agree with the fp64 ones (coord_mode 0) to binary32 rounding: a location
+    moves by at most a few units of 2^-24, i.e. a few 1e-5 pixels on a level
+    167 pixels wide, so the fused forward of a tiny and of a decoder-shaped
+    problem (levels with W != H) match to 2e-5 relative L2.  Dividing by
+    (H, W), or summing before dividing, moves samples by whole pixels and
+    fails this."""
+    rng = np.random.default_rng(34)
+    cases = [_fused_problem(rng),
+             _fused_problem(rng, B=1, Q=24, M=4, D=4, K=4, shapes=((100, 167), (50, 84), (25, 42), (13, 21)),
+                            spread=3.0)]
+    for f in cases:
+        f = {k: (v.astype(np.float32).astype(np.float64) if v.dtype == np.float64 else v) for k, v in f.items()}
+        a = oracle.fused_forward(f, "f64", coord_mode=1)
+        b = oracle.fused_forward(f, "f64", coord_mode=0)
+        err = float(np.linalg.norm(a - b) / np.linalg.norm(b))
+        assert err <= 2e-5, f"fused coordinate modes differ: rel-L2 {err:.3e}"
+        la = oracle.fused_locations(f["reference_points"], f["sampling_offsets"], f["spatial_shapes"], 1)
+        lb = oracle.fused_locations(f["reference_points"], f["sampling_offsets"], f["spatial_shapes"], 0)
+        assert np.max(np.abs(la - lb)) <= 2.0 ** -20, "binary32 fused locations far from the fp64 ones"
+
+
+def pin_fused_fp32_location():
+    """coord_mode 1 forms loc = ref + off / W with two binary32 roundings (the
+    quotient, then the sum).  For ref = 0.70616740 and off = -0.61850226 on a
+    level three pixels wide (both binary32 values), the quotient rounds to the
+    nearest binary32 and the sum then rounds to exactly 0.5, the centre of
+    pixel 1, so the fused output is A * value[pixel 1] = 20 exactly.  The exact
+    fp64 location, and a single rounding of it, are both just below 0.5 and
+    pick the cell [0, 1].  The same values on the y axis of a level three
+    pixels high fix the division by H."""
+    r = float(np.float32(0.7061673998832703))
+    o = float(np.float32(-0.6185022592544556))
+    value = np.array([10.0, 20.0, 40.0]).reshape(1, 3, 1, 1)
+    for axis, shapes in ((0, ((1, 3),)), (1, ((3, 1),))):
+        ref = np.full((1, 1, 1, 2), 0.5)
+        off = np.zeros((1, 1, 1, 1, 1, 2))
+        ref[..., axis] = r
+        off[..., axis] = o
+        f = {"value": value, "spatial_shapes": np.asarray(shapes, dtype=np.int64),
+             "level_start_index": np.zeros(1, dtype=np.int64), "reference_points": ref, "sampling_offsets": off,
+             "attention_logits": np.zeros((1, 1, 1, 1)), "grad_out": np.ones((1, 1, 1))}
+        loc = oracle.fused_locations(ref, off, f["spatial_shapes"], 1)
+        assert loc[0, 0, 0, 0, 0, axis] == 0.5, f"binary32 fused location {loc.ravel()}"
+        out1 = oracle.fused_forward(f, "f64", coord_mode=1)
+        assert out1.ravel()[0] == 20.0, f"axis {axis}: fused binary32 output {out1.ravel()}"
+        out0 = oracle.fused_forward(f, "f64", coord_mode=0)
+        assert 19.99 < out0.ravel()[0] < 20.0, f"axis {axis}: fused fp64 output {out0.ravel()}"
+
+
 ALL_PINS = [
     pin_hand_worked, pin_constant_field, pin_linear_field, pin_pixel_centres, pin_zero_padding,
     pin_convexity, pin_gridsample, pin_brute_force, pin_finite_differences, pin_adjoint,
     pin_scatter_total, pin_fp32_coordinate, pin_coordinate_modes_agree, pin_samplers,
     pin_fused_special_cases, pin_fused_torch_restatement, pin_fused_finite_differences,
+    pin_fused_coordinate_modes_agree, pin_fused_fp32_location,
 ]

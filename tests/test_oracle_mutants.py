@@ -1,7 +1,9 @@
 """Plant plausible mistakes in a copy of the C oracle and check that the pins
 catch each one: a wrong sign, a swapped index or axis, a dropped factor or
 term, an off-by-one bound, trunc for floor, the fp64 coordinate in place of the
-binary32 one.  CPU only."""
+binary32 one, and in the fused locations a sum taken before the division,
+(H, W) for (W, H), one rounding in place of two, or a flipped offset.  CPU
+only."""
 import os
 import subprocess
 import sys
@@ -41,6 +43,13 @@ MUTANTS = [
     ("fp32_mode_ignored", "if (P->coord_mode == 1) {", "if (0) {"),
     ("unit_q_index", "int64_t p = (((b * P->Q + q) * P->M + m) * P->L + l) * P->K + k;",
      "int64_t p = (((b * P->Q + q) * P->M + m) * P->L + k) * P->K + l;"),
+    # fused locations in binary32 (coord_mode 1)
+    ("fused_sum_before_divide", "float quot = (float)o / (float)size[c];\n                                float sum = (float)r[c] + quot;",
+     "float sum = ((float)r[c] + (float)o) / (float)size[c];"),
+    ("fused_divide_by_hw", "float quot = (float)o / (float)size[c];", "float quot = (float)o / (float)size[1 - c];"),
+    ("fused_one_rounding", "float quot = (float)o / (float)size[c];\n                                float sum = (float)r[c] + quot;",
+     "float sum = (float)(r[c] + o / size[c]);"),
+    ("fused_offset_sign", "float sum = (float)r[c] + quot;", "float sum = (float)r[c] - quot;"),
 ]
 
 
