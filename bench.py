@@ -1,7 +1,8 @@
 """Benchmark of the MSDA sampling core (forward + backward) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decoder_bf16] [--accum fp32|native|auto] [--all]
+                    [--workload stress_bf16] [--accum fp32|native|auto|deterministic]
+                    [--all] [--fused] [--no-configs]
 
 One step = one pass of the whole hot path over one batch: forward
 (msda_forward), then backward (msda_backward: zero or widen of the grad_value
@@ -10,6 +11,13 @@ rounding pass).  Inputs are resident in HBM; the L2 is flushed (a read of a
 512 MB buffer) between steps, outside the timed events.  The metric is (b, q, m)
 output vectors per second over the timed steps (higher is better).
 
+The contract line runs the largest single-GPU workload, stress_bf16 (B=8,
+Q=20000, a 768x1024 pyramid of 4 levels, M=8, D=32, L=K=4, bf16) with the
+FP32 grad_value accumulator it asks for.  Its K timed steps run untraced;
+per-kernel durations (`kernels`, `roofline`) come from a separate traced pass
+after them.  `all_configs` holds the other named workloads, each timed on its
+own inputs, and `dispatch` the host time per call of the autograd operator.
+
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (weak scaling, no data-path collective: the path shards over batches); the
 step time is the max over ranks and the value is the units of all ranks over
@@ -17,8 +25,9 @@ that time.
 
 --impl reference times the fp64 CPU oracle (test infrastructure) on the host
 cores on a bounded sample of the same workload.
---all prints one extra JSON line per named workload with forward, backward and
-fwd+bwd times (not the contract line).
+--all prints one extra JSON line per named workload with every accumulator
+(not the contract line); --fused the fused operator against PyTorch ops
+around the core.
 """
 from __future__ import annotations
 
@@ -49,10 +58,22 @@ FALLBACK_HBM_GBS = 6800.0
 # byte models (algorithmic bytes per launch): per-corner (every in-level
 # corner row counted each time) and unique (each distinct value row once)
 
+_corner_memo = {}
+
+
 def corner_counts(wl: W.Workload, inp, unique: bool = True):
     """(in-bounds (sample, corner) pairs, distinct value rows they touch), on
     the binary32 pixel coordinate the kernels use.  A value row is one
-    (b, pixel, m): D contiguous channels."""
+    (b, pixel, m): D contiguous channels.  Remembered per workload and input
+    set within the run."""
+    key = (wl, id(inp["sampling_locations"]), unique)
+    if key not in _corner_memo:
+        _corner_memo.clear()
+        _corner_memo[key] = _corner_counts(wl, inp, unique)
+    return _corner_memo[key]
+
+
+def _corner_counts(wl: W.Workload, inp, unique: bool):
     loc = W.to_f64(inp["sampling_locations"], wl.dtype)         # [B,Q,M,L,K,2]
     B, Q, M = loc.shape[:3]
     starts = W.level_start_index(wl.shapes)
@@ -260,22 +281,17 @@ class GpuStep:
         # writing back someone else's dirty lines
         self.flush_sink = self.flush_buf.sum()
 
-    def timed(self, fn, steps: int, trace_every: int = 0):
-        """Device time of `fn` per step with the L2 flushed before each one (ms).
-        With trace_every = n > 0 the library's kernel trace records every n-th
-        step only (its event pairs serialise the kernels of the step they
-        bracket, so tracing every step would slow the step being measured)."""
+    def timed(self, fn, steps: int):
+        """Device time of `fn` per step with the L2 flushed before each one (ms):
+        CUDA events on the launching stream around each call, the flush
+        outside them."""
         torch = self.torch
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-        for i, (a, b) in enumerate(ev):
-            if trace_every:
-                self.msda.trace_pause(i % trace_every != 0)
+        for a, b in ev:
             self.flush()
             a.record()
             fn()
             b.record()
-        if trace_every:
-            self.msda.trace_pause(False)
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in ev]
 
@@ -378,6 +394,65 @@ def graph_cross_check(st, steps: int):
             "stream_ms_per_step": round(sum(stream) / steps, 5)}
 
 
+def l2_bytes(device) -> int:
+    import torch
+
+    return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (126 << 20))
+
+
+def bound_of(kernel: str, wl: W.Workload, accum: str, l2: int) -> str:
+    """The ceiling that binds a kernel of this workload: HBM when its gathers
+    (value) or its accumulator spill past the L2, else the L2 itself, for the
+    backward its rate of reduction operations."""
+    es = W.ESIZE[wl.dtype]
+    value_bytes = wl.B * wl.S * wl.M * wl.D * es
+    acc_bytes = wl.B * wl.S * wl.M * wl.D * (4 if accum == "fp32" else es)
+    if kernel in ("zero", "convert"):
+        return "hbm" if acc_bytes > l2 else "l2"
+    if value_bytes > l2 or (kernel == "backward" and acc_bytes > l2):
+        return "hbm"
+    return "l2_reductions" if kernel == "backward" else "l2"
+
+
+def kernel_table(recs):
+    """Per-kernel launches, mean duration and share of a traced pass."""
+    per = {}
+    for name, ms, work in recs:
+        per.setdefault(name, []).append(ms)
+    tot = sum(sum(v) for v in per.values()) or 1.0
+    return per, {k: {"launches": len(v), "avg_ms": round(statistics.mean(v), 5), "share": round(sum(v) / tot, 4)}
+                 for k, v in per.items()}
+
+
+def traced_pass(st, steps: int):
+    """Per-kernel durations: `steps` further steps with the library's kernel
+    trace on (an event pair around every launch, no programmatic launches).
+    Separate from the headline steps, which run untraced."""
+    msda = st.msda
+    msda.trace_enable(16 * steps + 16)
+    st.timed(st.step, steps)
+    recs, dropped = msda.trace_read()
+    msda.trace_enable(0)
+    return recs, dropped
+
+
+def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2: int, kernels: dict):
+    peak, peak_kind = peaks()
+    avg_ms = statistics.mean(per[dom])
+    alg = model["convert"] if dom == "convert" else model[dom]
+    achieved = alg / (avg_ms / 1e3) / 1e9
+    roof = {"kernel": dom, "bound": bound_of(dom, wl, accum, l2), "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom, wl.name, accum),
+            "algorithmic_bytes": alg, "bytes_model": "per-corner (every in-level corner row each time)",
+            "avg_launch_ms": round(avg_ms, 5), "peak_source": peak_kind, "launches_traced": len(per[dom])}
+    uf = unique_fractions(model, kernels, peak)
+    if uf:
+        roof["compulsory_frac"] = uf["backward_frac"] if dom in ("backward", "zero", "convert") else uf["forward_frac"]
+        roof["compulsory_scope"] = ("backward pass (zero + kernel + convert)" if dom != "forward"
+                                    else "forward pass")
+    return roof
+
+
 def run_ours(args):
     import torch
 
@@ -393,78 +468,73 @@ def run_ours(args):
     inp = W.make_inputs(wl)
     accum = args.accum or wl.accum
     st = GpuStep(wl, inp, accum, device)
+    resolved = st.resolved
     corners, urows = corner_counts(wl, inp)
     model = byte_model(wl, corners, urows)
-    red_ceiling = reduction_ceiling_for(st.resolved, wl.dtype)
+    red_ceiling = reduction_ceiling_for(resolved, wl.dtype)
+    l2 = l2_bytes(device)
 
     for _ in range(max(args.warmup, 3)):
         st.flush()
         st.step()
     torch.cuda.synchronize()
-    # launches per step, from one traced step
+    # launches per step, from one traced step outside the timed region
     msda.trace_enable(64)
     st.step()
     recs, _ = msda.trace_read()
+    msda.trace_enable(0)
     launches_per_step = len(recs)
 
-    # trace one step in 64 (at least 8 traced steps): a traced step runs its
-    # kernels without programmatic launches and with events between them, so
-    # each costs the headline time it is part of
-    trace_every = args.trace_every if args.trace_every > 0 else max(1, min(64, args.steps // 8))
-    msda.trace_enable(4 * (args.steps // trace_every + 2))
+    # headline: the timed steps run untraced, with programmatic launches
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     with ClockSampler(uuid) as clk:
-        times = st.timed(st.step, args.steps, trace_every=trace_every)
+        times = st.timed(st.step, args.steps)
     torch.cuda.synchronize()
-    recs, dropped = msda.trace_read()
-    msda.trace_enable(0)
     total_ms = max_over_ranks(float(sum(times)), dist, device)
     ms_per_step = total_ms / args.steps
     value = job_throughput(wl.units, world, args.steps, total_ms)
 
-    # per-kernel durations over the traced part of the timed region
-    per = {}
-    for name, ms, work in recs:
-        per.setdefault(name, []).append(ms)
+    # per-kernel durations from a separate traced pass
+    recs, dropped = traced_pass(st, max(4, min(args.steps, args.trace_steps)))
+    per, kernels = kernel_table(recs)
     dom = max(per, key=lambda k: sum(per[k])) if per else None
-    peak, peak_kind = peaks()
-    roof = None
-    if dom:
-        avg_ms = statistics.mean(per[dom])
-        alg = model["convert"] if dom == "convert" else model[dom]
-        achieved = alg / (avg_ms / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom, wl.name, st.resolved),
-                "algorithmic_bytes": alg, "avg_launch_ms": round(avg_ms, 5), "peak_source": peak_kind,
-                "launches_traced": len(per[dom])}
-    kernels = {k: {"launches": len(v), "avg_ms": round(statistics.mean(v), 5),
-                   "share": round(sum(v) / sum(sum(x) for x in per.values()), 4)} for k, v in per.items()}
+    roof = roofline_of(dom, per, wl, model, resolved, l2, kernels) if dom else None
+    peak, _ = peaks()
 
     graph = graph_cross_check(st, min(args.steps, 2000)) if not args.no_graph else None
     e2e = run_e2e(st, inp, args) if not args.no_e2e else None
+    del st
+    torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(wl, inp, budget_s=args.cpu_seconds)
+    others = None
+    dispatch = None
+    if rank == 0 and not args.no_configs:
+        others = all_configs(args, device, wl.name, inp if wl.name == "stress_bf16" else None)
+        dispatch = dispatch_timing(device)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.B, "Q": wl.Qn, "M": wl.M, "D": wl.D, "L": wl.L, "K": wl.K,
-                       "S": wl.S, "spatial_shapes": [list(s) for s in wl.shapes], "accum": st.resolved,
+                       "S": wl.S, "spatial_shapes": [list(s) for s in wl.shapes], "accum": accum,
+                       "accum_resolved": resolved,
                        "l2": f"flushed between steps (read of a {FLUSH_BYTES >> 20} MB buffer, outside the timed events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
-            "roofline": roof, "kernels": kernels, "bytes_per_step_model": model["step"],
+            "roofline": roof, "kernels": kernels, "kernels_source": "separate traced pass after the timed steps",
+            "bytes_per_step_model": model["step"],
             "unique_model": unique_fractions(model, kernels, peak),
-            "reduction_roofline": reduction_roofline(wl, corners, st.resolved, kernels, red_ceiling),
+            "reduction_roofline": reduction_roofline(wl, corners, resolved, kernels, red_ceiling),
             "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
-            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "traced_steps_every": trace_every,
-            "graph_cross_check": graph,
+            "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "graph_cross_check": graph,
+            "all_configs": others, "dispatch": dispatch,
         }
         print(json.dumps(line), flush=True)
     if args.all and rank == 0:
@@ -476,6 +546,98 @@ def run_ours(args):
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def config_entry(wl: W.Workload, inp, accum: str, device, n: int, l2: int):
+    """Forward, backward and fwd+bwd device times (median of n, L2 flushed) of
+    one workload and accumulator, with both byte models' fractions of the
+    measured peak and the dominant kernel's bound."""
+    import torch
+
+    st = GpuStep(wl, inp, accum, device)
+    corners, urows = corner_counts(wl, inp)
+    model = byte_model(wl, corners, urows)
+    peak, _ = peaks()
+    for _ in range(3):
+        st.step()
+    tf = statistics.median(st.timed(st.forward, n))
+    tb = statistics.median(st.timed(st.backward, n))
+    ts = statistics.median(st.timed(st.step, n))
+    recs, _ = traced_pass(st, 4)
+    per, kernels = kernel_table(recs)
+    dom = max(per, key=lambda k: sum(per[k])) if per else None
+    e = {"accum": accum, "accum_resolved": st.resolved, "fwd_ms": round(tf, 4), "bwd_ms": round(tb, 4),
+         "step_ms": round(ts, 4), "step_units_per_s": round(wl.units / (ts / 1e3), 1),
+         "fwd_frac_per_corner": round(model["forward"] / (tf / 1e3) / 1e9 / peak, 4),
+         "bwd_frac_per_corner": round(model["bwd_total"] / (tb / 1e3) / 1e9 / peak, 4),
+         "fwd_frac_compulsory": round(model["forward_unique"] / (tf / 1e3) / 1e9 / peak, 4),
+         "bwd_frac_compulsory": round(model["bwd_total_unique"] / (tb / 1e3) / 1e9 / peak, 4),
+         "kernels": kernels,
+         "dominant": {"kernel": dom, "bound": bound_of(dom, wl, st.resolved, l2)} if dom else None}
+    del st
+    torch.cuda.empty_cache()
+    return e
+
+
+def all_configs(args, device, headline: str, headline_inp=None):
+    """The other named workloads (and the headline one's other accumulator),
+    each with its own inputs: every configuration in one run."""
+    l2 = l2_bytes(device)
+    res = {}
+    for name in ("tiny_fp32", "decoder_bf16", "encoder_fp16", "oddD_fp32", "stress_bf16"):
+        wl = W.WORKLOADS[name]
+        if name == headline:
+            if wl.dtype == "f32":
+                continue
+            inp = headline_inp if headline_inp is not None else W.make_inputs(wl)
+            accums = ["native"] if wl.accum == "fp32" else ["fp32"]
+        else:
+            inp = W.make_inputs(wl)
+            accums = ["auto"] + (["fp32"] if wl.dtype != "f32" else [])
+        n = 5 if name == "stress_bf16" else 30
+        res[name] = {"units": wl.units,
+                     "runs": [config_entry(wl, inp, a, device, n, l2) for a in accums]}
+        del inp
+    return res
+
+
+def dispatch_timing(device, calls: int = 200):
+    """Dispatch-inclusive time per call on the decoder workload: `calls`
+    back-to-back forward + backward calls through the autograd operator
+    (multi_scale_deformable_attention, device-resident inputs and shapes), one
+    synchronisation at the end; beside the same calls through the raw C ABI.
+    host_us: time until the loop has enqueued every call; wall_us: until the
+    GPU has finished them."""
+    import torch
+
+    import scale_deformable_attention_gb300 as msda
+
+    wl = W.WORKLOADS["decoder_bf16"]
+    inp = W.make_inputs(wl)
+    t = W.to_torch(inp, wl.dtype, device)
+    leaves = [t[k].clone().requires_grad_(True) for k in ("value", "sampling_locations", "attention_weights")]
+    ss, lsi, g = t["spatial_shapes"], t["level_start_index"], t["grad_out"]
+
+    def autograd_call():
+        out = msda.multi_scale_deformable_attention(leaves[0], ss, lsi, leaves[1], leaves[2])
+        out.backward(g)
+
+    st = GpuStep(wl, inp, "auto", device)
+    res = {"workload": wl.name, "calls": calls}
+    for tag, fn in (("autograd_op", autograd_call), ("c_abi", st.step)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        t2 = time.perf_counter()
+        res[tag] = {"host_us_per_call": round((t1 - t0) / calls * 1e6, 2),
+                    "wall_us_per_call": round((t2 - t0) / calls * 1e6, 2)}
+    del st
+    return res
 
 
 def run_e2e(st: GpuStep, inp, args):
@@ -550,21 +712,40 @@ def run_e2e(st: GpuStep, inp, args):
             "pipelining": "double-buffered: upload i+1 and download i-1 overlap compute i"}
 
 
+def oracle_sample(wl: W.Workload, inp, queries: int):
+    """Batch 0 and its first `queries` queries: a bounded sample of the
+    workload for the oracle (its grad_value is then one batch image)."""
+    q = int(max(1, min(wl.Qn, queries)))
+    sub = {"value": inp["value"][:1], "spatial_shapes": inp["spatial_shapes"],
+           "level_start_index": inp["level_start_index"]}
+    for k in ("sampling_locations", "attention_weights", "grad_out"):
+        sub[k] = np.ascontiguousarray(inp[k][:1, :q])
+    return sub, q, q * wl.M
+
+
 def cpu_baseline(wl: W.Workload, inp, budget_s: float):
-    """The fp64 oracle on the host cores, on whole fwd+bwd passes of the same
-    inputs repeated for about `budget_s` seconds."""
+    """The fp64 oracle on the host cores: whole fwd+bwd passes over a bounded
+    sample of the same inputs (batch 0, a prefix of its queries sized so one
+    pass takes about a second), repeated for about `budget_s` seconds."""
     import oracle
 
+    sub, q, units = oracle_sample(wl, inp, min(wl.Qn, 256))
+    t0 = time.perf_counter()
+    oracle.forward(sub, wl.dtype)
+    oracle.backward(sub, wl.dtype)
+    t1 = time.perf_counter() - t0
+    sub, q, units = oracle_sample(wl, inp, q * max(1.0, 1.0 / max(t1, 1e-3)))
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.forward(inp, wl.dtype)
-        oracle.backward(inp, wl.dtype)
+        oracle.forward(sub, wl.dtype)
+        oracle.backward(sub, wl.dtype)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": round(wl.units * reps / el, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{reps} full fwd+bwd passes of {wl.name} ({wl.units} units each) in {el:.1f} s"}
+    return {"value": round(units * reps / el, 1), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} fwd+bwd passes over batch 0, queries 0..{q - 1} of {wl.Qn} ({units} units each) "
+                      f"of {wl.name}, in {el:.1f} s"}
 
 
 def run_workload_table(name: str, args, device):
@@ -723,17 +904,15 @@ def run_reference(args):
 
     wl = W.WORKLOADS[args.workload]
     inp = W.make_inputs(wl)
-    # size each step's sample (a prefix of the queries) so the run takes ~budget
+    # each step is one fwd+bwd pass of the oracle over batch 0 and a prefix of
+    # its queries, sized so that warm-up and timed steps take about ref_budget
+    sub, q, units = oracle_sample(wl, inp, min(wl.Qn, 64))
     t0 = time.perf_counter()
-    oracle.forward(inp, wl.dtype)
-    oracle.backward(inp, wl.dtype)
-    t_full = time.perf_counter() - t0
+    oracle.forward(sub, wl.dtype)
+    oracle.backward(sub, wl.dtype)
+    t_probe = time.perf_counter() - t0
     per_step = args.ref_budget / max(1, args.steps + args.warmup)
-    q = int(max(1, min(wl.Qn, wl.Qn * per_step / max(t_full, 1e-9))))
-    sub = dict(inp)
-    for k in ("sampling_locations", "attention_weights", "grad_out"):
-        sub[k] = np.ascontiguousarray(inp[k][:, :q])
-    units = wl.B * q * wl.M
+    sub, q, units = oracle_sample(wl, inp, q * per_step / max(t_probe, 1e-6))
     for _ in range(args.warmup):
         oracle.forward(sub, wl.dtype)
         oracle.backward(sub, wl.dtype)
@@ -743,7 +922,7 @@ def run_reference(args):
         oracle.backward(sub, wl.dtype)
     el = time.perf_counter() - t0
     value = units * args.steps / el
-    sample = f"first {q} of {wl.Qn} queries of every batch ({units} units) per step"
+    sample = f"batch 0, queries 0..{q - 1} of {wl.Qn} ({units} (b,q,m) units) per step"
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -759,10 +938,10 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decoder_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="stress_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch size B")
     ap.add_argument("--accum", choices=["auto", "native", "fp32", "deterministic"], default=None,
                     help="grad_value accumulator (default: the workload's)")
@@ -773,8 +952,10 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay cross-check")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--trace-every", type=int, default=0,
-                    help="record per-kernel events on every n-th timed step (0: one in 64, at least 8 steps)")
+    ap.add_argument("--trace-steps", type=int, default=16,
+                    help="steps of the separate traced pass that gives per-kernel durations")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' entries (all_configs) and the dispatch timing")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
     args = ap.parse_args(argv)

@@ -236,13 +236,23 @@ msda_status msda_backward_fused(msda_dtype dt, msda_accum mode, unsigned flags, 
  * allocation after start-up).  Results equal msda_backward(dt,
  * MSDA_ACCUM_FP32, flags, ...) up to the summation order of grad_value.
  *
- * Limit: B*S*M*D <= MSDA_STATIC_WORKSPACE_BYTES / 4 for fp16 / bf16, else
- * MSDA_ERR_WORKSPACE before anything is enqueued (fp32 I/O needs no scratch
- * and has no limit).  Every GPU on which it is called holds the array until
- * the process exits.  The first call on a device looks up the array's device
- * address; make it before any stream capture.  All calls share the one
- * array: calls that can overlap on the GPU race and must be serialised by the
- * caller.  Other arguments and errors as msda_backward.
+ * Limit: the scratch that msda_backward_workspace_size(dt, MSDA_ACCUM_FP32,
+ * ...) reports must fit in MSDA_STATIC_WORKSPACE_BYTES, else
+ * MSDA_ERR_WORKSPACE before anything is enqueued.  The limit applies only to
+ * calls that need scratch: fp32 I/O, and calls with nothing to sample
+ * (B*Q*M*D == 0), need none and have no limit.  Arguments are checked as
+ * msda_backward checks them, and give its errors.
+ *
+ * The array occupies MSDA_STATIC_WORKSPACE_BYTES on every device where the
+ * translation unit that holds it is loaded, until the process exits: with
+ * lazy module loading (the CUDA default) a device on which this entry point
+ * has looked the array up, with CUDA_MODULE_LOADING=EAGER every device the
+ * process creates a context on, whether or not this entry point is called.  Its device
+ * address is looked up on every call made outside stream capture; a call
+ * made while `stream` is being captured uses the address found by the last
+ * uncaptured call on that device, so make one such call first.  All calls
+ * share the one array: calls that can overlap on the GPU race and must be
+ * serialised by the caller.  Other arguments and errors as msda_backward.
  */
 #define MSDA_STATIC_WORKSPACE_BYTES (64u << 20)
 msda_status msda_backward_static_workspace(msda_dtype dt, unsigned flags, int64_t B, int64_t S, int64_t M, int64_t D,

@@ -24,6 +24,8 @@ Entry points:
 from __future__ import annotations
 
 import ctypes
+import threading
+import weakref
 from typing import Optional, Tuple
 
 import torch
@@ -44,6 +46,67 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
+
+
+# Host-side checks of spatial_shapes without a per-call host synchronisation.
+# A CPU tensor is checked directly and copied to the device once; a device
+# tensor is read back once, the first time it is seen.  Both results are
+# remembered per tensor object and its version counter (an in-place change
+# invalidates them), and forgotten when the tensor is freed.  The kernels check
+# every level on the device as well, so a shape that escapes these host checks
+# reads nothing out of bounds: it is treated as empty and raises device error
+# bit 0.
+_seen_lock = threading.Lock()
+_shapes_ok = {}      # id(tensor) -> (weakref, version, S)
+_device_copy = {}    # (id(tensor), device) -> (weakref, version, device tensor)
+_CACHE_MAX = 256
+
+
+def _remember(table, key, t, payload):
+    with _seen_lock:
+        if len(table) >= _CACHE_MAX:
+            table.clear()
+        table[key] = (weakref.ref(t), t._version, payload)
+
+
+def _recall(table, key, t):
+    with _seen_lock:
+        e = table.get(key)
+    if e is not None and e[0]() is t and e[1] == t._version:
+        return e[2]
+    return None
+
+
+def _check_shapes(spatial_shapes: torch.Tensor, S: int) -> None:
+    if spatial_shapes.device.type != "cpu" and _recall(_shapes_ok, id(spatial_shapes), spatial_shapes) == S:
+        return
+    if spatial_shapes.device.type != "cpu" and torch.cuda.is_current_stream_capturing():
+        raise RuntimeError("spatial_shapes on the device cannot be checked while a CUDA graph is being captured: "
+                           "make one call with it before capturing, or pass validate=False")
+    hw = spatial_shapes.to("cpu", torch.int64)     # a device tensor syncs here, once
+    if bool((hw <= 0).any()):
+        raise ValueError(f"spatial_shapes must be positive, got {hw.tolist()}")
+    tot = int((hw[:, 0] * hw[:, 1]).sum())
+    if tot != S:
+        raise ValueError(f"value has S={S} rows but sum(H*W) over spatial_shapes is {tot}")
+    if spatial_shapes.device.type != "cpu":
+        _remember(_shapes_ok, id(spatial_shapes), spatial_shapes, S)
+
+
+def _on_device(t: torch.Tensor, dev: torch.device) -> torch.Tensor:
+    """``t`` as a contiguous int64 tensor on ``dev``; a CPU tensor is copied once
+    (a copy from pageable host memory waits for the stream) and reused."""
+    if t.device == dev and t.dtype == torch.int64 and t.is_contiguous():
+        return t
+    if t.device.type == "cpu":
+        key = (id(t), str(dev))
+        hit = _recall(_device_copy, key, t)
+        if hit is not None:
+            return hit
+        d = t.to(dev, torch.int64).contiguous()
+        _remember(_device_copy, key, t, d)
+        return d
+    return t.to(dev, torch.int64).contiguous()
 
 
 def level_start_index_of(spatial_shapes: torch.Tensor) -> torch.Tensor:
@@ -79,19 +142,14 @@ def _prepare(value, spatial_shapes, level_start_index, sampling_locations, atten
     if spatial_shapes.dim() != 2 or spatial_shapes.shape != (L, 2):
         raise ValueError(f"spatial_shapes must be [L={L}, 2], got {tuple(spatial_shapes.shape)}")
     if validate:
-        hw = spatial_shapes.to("cpu", torch.int64)
-        if bool((hw <= 0).any()):
-            raise ValueError(f"spatial_shapes must be positive, got {hw.tolist()}")
-        tot = int((hw[:, 0] * hw[:, 1]).sum())
-        if tot != S:
-            raise ValueError(f"value has S={S} rows but sum(H*W) over spatial_shapes is {tot}")
-    spatial_shapes = spatial_shapes.to(dev, torch.int64).contiguous()
+        _check_shapes(spatial_shapes, S)
+    spatial_shapes = _on_device(spatial_shapes, dev)
     if level_start_index is None:
         level_start_index = level_start_index_of(spatial_shapes)
     else:
         if level_start_index.shape != (L,):
             raise ValueError(f"level_start_index must be [L={L}], got {tuple(level_start_index.shape)}")
-        level_start_index = level_start_index.to(dev, torch.int64).contiguous()
+        level_start_index = _on_device(level_start_index, dev)
     dims = (B, S, M, D, L, K, Q)
     return (value.contiguous(), spatial_shapes, level_start_index, sampling_locations.contiguous(),
             attention_weights.contiguous(), dims)
@@ -172,8 +230,8 @@ class _MSDAFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, value, spatial_shapes, level_start_index, sampling_locations, attention_weights, accum):
         out = forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights)
-        ss = spatial_shapes.to(value.device, torch.int64)
-        lsi = level_start_index_of(ss) if level_start_index is None else level_start_index.to(value.device, torch.int64)
+        ss = _on_device(spatial_shapes, value.device)
+        lsi = level_start_index_of(ss) if level_start_index is None else _on_device(level_start_index, value.device)
         ctx.save_for_backward(value, ss, lsi, sampling_locations, attention_weights)
         ctx.accum = accum
         return out
@@ -272,8 +330,8 @@ class _MSDAFusedFunction(torch.autograd.Function):
                 attention_logits, accum):
         out = forward_fused(value, spatial_shapes, level_start_index, reference_points, sampling_offsets,
                             attention_logits)
-        ss = spatial_shapes.to(value.device, torch.int64)
-        lsi = level_start_index_of(ss) if level_start_index is None else level_start_index.to(value.device, torch.int64)
+        ss = _on_device(spatial_shapes, value.device)
+        lsi = level_start_index_of(ss) if level_start_index is None else _on_device(level_start_index, value.device)
         ctx.save_for_backward(value, ss, lsi, reference_points, sampling_offsets, attention_logits)
         ctx.accum = accum
         return out

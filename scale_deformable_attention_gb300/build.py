@@ -11,7 +11,9 @@ from __future__ import annotations
 import argparse
 import fcntl
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -41,11 +43,26 @@ def _deps():
         os.path.abspath(__file__)]
 
 
+STAMP = LIB + ".stamp"
+
+
+def _stamp() -> str:
+    """Digest of every source the library is built from, of the build flags and
+    of the machine it is built on: a library built elsewhere, or from other
+    sources, is rebuilt whatever its file times say."""
+    h = hashlib.sha256()
+    for p in sorted(_deps()):
+        with open(p, "rb") as f:
+            h.update(os.path.relpath(p, ROOT).encode() + b"\0" + f.read())
+    h.update(" ".join(ARCH).encode() + platform.machine().encode())
+    return h.hexdigest()
+
+
 def stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(p) > t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() != _stamp()
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
@@ -87,6 +104,9 @@ def _build_locked(verbose: bool, ptxas_info: bool) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
     os.replace(tmp, LIB)
+    with open(STAMP + ".tmp", "w") as f:
+        f.write(_stamp())
+    os.replace(STAMP + ".tmp", STAMP)
     return LIB
 
 

@@ -68,3 +68,28 @@ def test_byte_model_formula(bench):
     assert m["bwd_total"] == m["backward"] + n_value * es
     assert m["forward_unique"] == rows * wl.D * es + samples * 3 * es + out
     assert m["bwd_total_unique"] == rows * wl.D * es + out + 2 * samples * 3 * es + n_value * es
+
+
+def test_bound_labels(bench):
+    """The roofline's bound names the ceiling that binds: HBM when value (or the
+    fp32 accumulator) exceeds the L2, else the L2 (its reduction rate for the
+    backward)."""
+    l2 = 126 << 20
+    stress = W.WORKLOADS["stress_bf16"]
+    decoder = W.WORKLOADS["decoder_bf16"]
+    assert bench.bound_of("backward", stress, "fp32", l2) == "hbm"
+    assert bench.bound_of("forward", stress, "fp32", l2) == "hbm"
+    assert bench.bound_of("backward", decoder, "native", l2) == "l2_reductions"
+    assert bench.bound_of("forward", decoder, "native", l2) == "l2"
+    assert bench.bound_of("zero", decoder, "fp32", l2) == "l2"
+    assert bench.bound_of("convert", stress, "fp32", l2) == "hbm"
+
+
+def test_oracle_sample_is_batch0_prefix(bench):
+    wl = W.WORKLOADS["decoder_bf16"].with_(B=2, Q=10)
+    inp = W.make_inputs(wl)
+    sub, q, units = bench.oracle_sample(wl, inp, 4.7)
+    assert q == 4 and units == 4 * wl.M
+    assert sub["value"].shape[0] == 1 and sub["sampling_locations"].shape[:2] == (1, 4)
+    assert np.array_equal(sub["grad_out"], inp["grad_out"][:1, :4])
+    assert bench.oracle_sample(wl, inp, 1e9)[1] == wl.Qn

@@ -58,3 +58,92 @@ def test_graph_replay_matches_eager(dtype, accum):
         assert torch.equal(captured[2], eager[2]) and torch.equal(captured[3], eager[3])
         assert rel_l2(f64(captured[1]), f64(eager[1])) <= tol
     assert msda.device_errors() == 0
+
+
+@pytest.mark.parametrize("shapes_on", ["cuda", "cpu"])
+def test_autograd_op_needs_no_host_sync(shapes_on):
+    """The differentiable operator (README, "Quickstart") checks spatial_shapes
+    on the host the first time it sees the tensor only: later forward +
+    backward calls make no synchronising call (torch's sync debug mode turns
+    one into an error)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import scale_deformable_attention_gb300 as msda
+
+    wl, t = _inputs("bf16", 34)
+    ss = t["spatial_shapes"].to(shapes_on)
+    leaves = [t[k].clone().requires_grad_(True) for k in ("value", "sampling_locations", "attention_weights")]
+
+    def run():
+        out = msda.multi_scale_deformable_attention(leaves[0], ss, None, leaves[1], leaves[2])
+        out.backward(t["grad_out"])
+        return out
+
+    run()                               # first sight of ss: checked (and copied) once
+    torch.cuda.synchronize()
+    torch.cuda.set_sync_debug_mode("error")
+    try:
+        for _ in range(3):
+            run()
+    finally:
+        torch.cuda.set_sync_debug_mode("default")
+    torch.cuda.synchronize()
+    bad = torch.tensor([[3, 3]] + [[1, 1]] * (wl.L - 1), dtype=torch.int64)
+    with pytest.raises(ValueError):
+        msda.multi_scale_deformable_attention(leaves[0], bad.to(shapes_on), None, leaves[1], leaves[2])
+
+
+def test_autograd_op_graph_capture():
+    """Forward + backward through the autograd operator captured as one CUDA
+    graph (README, "Caveats": graph capturable) and replayed on new inputs
+    copied into the captured leaves; compared with eager autograd calls."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import scale_deformable_attention_gb300 as msda
+
+    wl, t = _inputs("bf16", 35)
+    ss, lsi = t["spatial_shapes"], t["level_start_index"]
+    names = ("value", "sampling_locations", "attention_weights")
+    leaves = {k: t[k].clone().requires_grad_(True) for k in names}
+    gout = t["grad_out"].clone()
+
+    def run():
+        out = msda.multi_scale_deformable_attention(leaves["value"], ss, lsi, leaves["sampling_locations"],
+                                                    leaves["attention_weights"])
+        out.backward(gout)
+        return out
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            for v in leaves.values():
+                v.grad = None
+            run()
+    torch.cuda.current_stream().wait_stream(s)
+    for v in leaves.values():
+        v.grad = None
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        captured = run()
+
+    for seed in (36, 37):
+        _, fresh = _inputs("bf16", seed)
+        with torch.no_grad():
+            for k in names:
+                leaves[k].copy_(fresh[k])
+        gout.copy_(fresh["grad_out"])
+        g.replay()
+        torch.cuda.synchronize()
+        got = [captured.clone()] + [leaves[k].grad.clone() for k in names]
+        eager_leaves = {k: fresh[k].clone().requires_grad_(True) for k in names}
+        out = msda.multi_scale_deformable_attention(eager_leaves["value"], ss, lsi,
+                                                    eager_leaves["sampling_locations"],
+                                                    eager_leaves["attention_weights"])
+        out.backward(fresh["grad_out"])
+        torch.cuda.synchronize()
+        assert torch.equal(got[0], out.detach()), "forward differs between graph replay and eager"
+        assert torch.equal(got[2], eager_leaves["sampling_locations"].grad)
+        assert torch.equal(got[3], eager_leaves["attention_weights"].grad)
+        assert rel_l2(f64(got[1]), f64(eager_leaves["value"].grad)) <= 1e-2
+    assert msda.device_errors() == 0
