@@ -116,7 +116,16 @@ def byte_model(wl: W.Workload, corners: int, unique_rows=None) -> dict:
     bwd_kernel = 2 * gather + rowio + 2 * (loc + attn)
     bwd = bwd_kernel + n_value * es          # + one full grad_value write
     out = {"forward": fwd, "backward": bwd_kernel, "bwd_total": bwd, "zero": n_value * es,
-           "convert": n_value * (4 + es), "step": fwd + bwd}
+           "convert": n_value * (4 + es), "step": fwd + bwd,
+           # the FP32 accumulator on chip splits the backward kernel: the gather
+           # kernel (corner reads, grad_out, params, param grads) and the
+           # accumulate pass (the per-corner payload, summed in shared memory,
+           # and one full grad_value write); count and place read the locations
+           # (place writes a 4-byte entry per point and tile, about one)
+           "backward_gather": gather + rowio + 2 * (loc + attn),
+           "tile_accum": gather + n_value * es,
+           "tile_count": loc, "tile_place": loc + 4 * wl.samples,
+           "tile_scan": 12 * wl.B * wl.M * ((wl.S + 511) // 512)}
     if unique_rows is not None:
         urow = unique_rows * wl.D * es
         out["unique_rows"] = unique_rows
@@ -400,7 +409,7 @@ def l2_bytes(device) -> int:
     return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0) or (126 << 20))
 
 
-def bound_of(kernel: str, wl: W.Workload, accum: str, l2: int) -> str:
+def bound_of(kernel: str, wl: W.Workload, accum: str, l2: int, tiled: bool = False) -> str:
     """The ceiling that binds a kernel of this workload: HBM when its gathers
     (value) or its accumulator spill past the L2, else the L2 itself, for the
     backward its rate of reduction operations."""
@@ -409,9 +418,13 @@ def bound_of(kernel: str, wl: W.Workload, accum: str, l2: int) -> str:
     acc_bytes = wl.B * wl.S * wl.M * wl.D * (4 if accum == "fp32" else es)
     if kernel in ("zero", "convert"):
         return "hbm" if acc_bytes > l2 else "l2"
+    if kernel == "tile_accum":
+        return "hbm" if value_bytes > l2 else "l2"
+    if kernel.startswith("tile_"):
+        return "hbm" if wl.samples * 3 * es > l2 else "l2"
     if value_bytes > l2 or (kernel == "backward" and acc_bytes > l2):
         return "hbm"
-    return "l2_reductions" if kernel == "backward" else "l2"
+    return "l2_reductions" if kernel == "backward" and not tiled else "l2"
 
 
 def kernel_table(recs):
@@ -439,9 +452,11 @@ def traced_pass(st, steps: int):
 def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2: int, kernels: dict):
     peak, peak_kind = peaks()
     avg_ms = statistics.mean(per[dom])
-    alg = model["convert"] if dom == "convert" else model[dom]
+    # the backward kernel without its scatter when the accumulate pass holds grad_value
+    alg = model["backward_gather"] if dom == "backward" and "tile_accum" in per else model[dom]
     achieved = alg / (avg_ms / 1e3) / 1e9
-    roof = {"kernel": dom, "bound": bound_of(dom, wl, accum, l2), "achieved": round(achieved, 1), "peak": peak,
+    roof = {"kernel": dom, "bound": bound_of(dom, wl, accum, l2, "tile_accum" in per), "achieved": round(achieved, 1),
+            "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom, wl.name, accum),
             "algorithmic_bytes": alg, "bytes_model": "per-corner (every in-level corner row each time)",
             "avg_launch_ms": round(avg_ms, 5), "peak_source": peak_kind, "launches_traced": len(per[dom])}
@@ -573,7 +588,7 @@ def config_entry(wl: W.Workload, inp, accum: str, device, n: int, l2: int):
          "fwd_frac_compulsory": round(model["forward_unique"] / (tf / 1e3) / 1e9 / peak, 4),
          "bwd_frac_compulsory": round(model["bwd_total_unique"] / (tb / 1e3) / 1e9 / peak, 4),
          "kernels": kernels,
-         "dominant": {"kernel": dom, "bound": bound_of(dom, wl, st.resolved, l2)} if dom else None}
+         "dominant": {"kernel": dom, "bound": bound_of(dom, wl, st.resolved, l2, "tile_accum" in per)} if dom else None}
     del st
     torch.cuda.empty_cache()
     return e
@@ -604,8 +619,9 @@ def all_configs(args, device, headline: str, headline_inp=None):
 def dispatch_timing(device, calls: int = 200):
     """Dispatch-inclusive time per call on the decoder workload: `calls`
     back-to-back forward + backward calls through the autograd operator
-    (multi_scale_deformable_attention, device-resident inputs and shapes), one
-    synchronisation at the end; beside the same calls through the raw C ABI.
+    (multi_scale_deformable_attention, device-resident inputs and shapes, the
+    leaves' gradients set to None before each call), one synchronisation at
+    the end; beside the same calls through the raw C ABI.
     host_us: time until the loop has enqueued every call; wall_us: until the
     GPU has finished them."""
     import torch
@@ -619,12 +635,20 @@ def dispatch_timing(device, calls: int = 200):
     ss, lsi, g = t["spatial_shapes"], t["level_start_index"], t["grad_out"]
 
     def autograd_call():
+        # a training step's pattern: gradients set to None before each backward
+        for v in leaves:
+            v.grad = None
         out = msda.multi_scale_deformable_attention(leaves[0], ss, lsi, leaves[1], leaves[2])
         out.backward(g)
 
+    def forward_call():
+        with torch.no_grad():
+            msda.multi_scale_deformable_attention(leaves[0], ss, lsi, leaves[1], leaves[2])
+
     st = GpuStep(wl, inp, "auto", device)
     res = {"workload": wl.name, "calls": calls}
-    for tag, fn in (("autograd_op", autograd_call), ("c_abi", st.step)):
+    for tag, fn in (("autograd_op", autograd_call), ("autograd_op_forward_only", forward_call),
+                    ("c_abi", st.step), ("c_abi_forward_only", st.forward)):
         for _ in range(5):
             fn()
         torch.cuda.synchronize()

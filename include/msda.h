@@ -316,7 +316,8 @@ typedef struct {
 } msda_trace_record;
 
 enum { MSDA_KERNEL_FORWARD = 0, MSDA_KERNEL_BACKWARD = 1, MSDA_KERNEL_ZERO = 2, MSDA_KERNEL_CONVERT = 3,
-       MSDA_KERNEL_COUNT = 4 };
+       MSDA_KERNEL_TILE_COUNT = 4, MSDA_KERNEL_TILE_SCAN = 5, MSDA_KERNEL_TILE_PLACE = 6,
+       MSDA_KERNEL_TILE_ACCUM = 7, MSDA_KERNEL_COUNT = 8 };
 
 msda_status msda_trace_enable(int capacity);
 /* Pause (paused != 0) or resume recording without destroying the events:

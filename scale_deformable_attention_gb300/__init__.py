@@ -59,6 +59,7 @@ def _stream(device: torch.device) -> int:
 _seen_lock = threading.Lock()
 _shapes_ok = {}      # id(tensor) -> (weakref, version, S)
 _device_copy = {}    # (id(tensor), device) -> (weakref, version, device tensor)
+_lsi_of = {}         # id(device spatial_shapes) -> (weakref, version, its level_start_index)
 _CACHE_MAX = 256
 
 
@@ -145,7 +146,10 @@ def _prepare(value, spatial_shapes, level_start_index, sampling_locations, atten
         _check_shapes(spatial_shapes, S)
     spatial_shapes = _on_device(spatial_shapes, dev)
     if level_start_index is None:
-        level_start_index = level_start_index_of(spatial_shapes)
+        level_start_index = _recall(_lsi_of, id(spatial_shapes), spatial_shapes)
+        if level_start_index is None:
+            level_start_index = level_start_index_of(spatial_shapes)
+            _remember(_lsi_of, id(spatial_shapes), spatial_shapes, level_start_index)
     else:
         if level_start_index.shape != (L,):
             raise ValueError(f"level_start_index must be [L={L}], got {tuple(level_start_index.shape)}")
@@ -178,8 +182,20 @@ def resolve_accum(dtype: torch.dtype, accum: str, dims) -> str:
     return _lib.ACCUM_NAMES[r]
 
 
-def workspace_size(dtype: torch.dtype, accum: str, dims) -> int:
-    return int(_lib.lib().msda_backward_workspace_size(DTYPE_CODE[dtype], ACCUM[accum], *dims))
+def workspace_size(dtype: torch.dtype, accum: str, dims, aligned: bool = True) -> int:
+    """Bytes of workspace the backward needs (C ABI ``msda_backward_workspace_size``).
+    The FP32 accumulator's figure assumes 16-byte aligned value, grad_out and
+    grad_value; ``aligned=False`` gives what it needs otherwise (the fp32
+    mirror of grad_value, B*S*M*D*4 bytes, when that is larger)."""
+    n = int(_lib.lib().msda_backward_workspace_size(DTYPE_CODE[dtype], ACCUM[accum], *dims))
+    if n and not aligned and resolve_accum(dtype, accum, dims) == "fp32":
+        B, S, M, D = dims[:4]
+        n = max(n, B * S * M * D * 4)
+    return n
+
+
+def _aligned16(*ts) -> bool:
+    return all(t.data_ptr() % 16 == 0 for t in ts)
 
 
 def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_index: Optional[torch.Tensor],
@@ -209,7 +225,7 @@ def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_inde
         raise ValueError("grad_value must be a contiguous tensor shaped and typed like value")
     grad_loc = torch.empty_like(loc)
     grad_attn = torch.empty_like(attn)
-    need = workspace_size(value.dtype, accum, dims)
+    need = workspace_size(value.dtype, accum, dims, _aligned16(value, grad_out, grad_value))
     if need and workspace is None:
         workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=value.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -222,25 +238,62 @@ def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_inde
     return grad_value, grad_loc, grad_attn
 
 
+_ws_bytes = {}   # (dtype, accum, dims) -> workspace bytes of an aligned call
+
+
+def _workspace_for(dtype, accum, dims) -> int:
+    key = (dtype, accum, dims)
+    n = _ws_bytes.get(key)
+    if n is None:
+        if len(_ws_bytes) >= _CACHE_MAX:
+            _ws_bytes.clear()
+        n = _ws_bytes[key] = workspace_size(dtype, accum, dims)
+    return n
+
+
 class _MSDAFunction(torch.autograd.Function):
     """Autograd wrapper (course ch. 5, "The autograd wrapper"): saves the inputs
     and recomputes the bilinear setup in the backward kernel; the backward is
-    not itself differentiable."""
+    not itself differentiable.  The inputs are checked once, in the forward;
+    both passes then call the C ABI directly (the dispatch cost per call is
+    what the README's "Benchmarks" measurement pitfalls are about)."""
 
     @staticmethod
     def forward(ctx, value, spatial_shapes, level_start_index, sampling_locations, attention_weights, accum):
-        out = forward(value, spatial_shapes, level_start_index, sampling_locations, attention_weights)
-        ss = _on_device(spatial_shapes, value.device)
-        lsi = level_start_index_of(ss) if level_start_index is None else _on_device(level_start_index, value.device)
-        ctx.save_for_backward(value, ss, lsi, sampling_locations, attention_weights)
+        value, ss, lsi, loc, attn, dims = _prepare(value, spatial_shapes, level_start_index, sampling_locations,
+                                                   attention_weights, True)
+        B, S, M, D, L, K, Q = dims
+        out = torch.empty((B, Q, M * D), dtype=value.dtype, device=value.device)
+        dev = value.device
+        with torch.cuda.device(dev):
+            _lib.check(_lib.lib().msda_forward(DTYPE_CODE[value.dtype], *dims, _ptr(value), _ptr(ss), _ptr(lsi),
+                                               _ptr(loc), _ptr(attn), _ptr(out), _stream(dev)))
+        ctx.save_for_backward(value, ss, lsi, loc, attn)
         ctx.accum = accum
+        ctx.dims = dims
         return out
 
     @staticmethod
     @torch.autograd.function.once_differentiable
     def backward(ctx, grad_out):
         value, ss, lsi, loc, attn = ctx.saved_tensors
-        gv, gl, ga = backward(value, ss, lsi, loc, attn, grad_out, accum=ctx.accum, validate=False)
+        dims = ctx.dims
+        if grad_out.dtype != value.dtype:
+            grad_out = grad_out.to(value.dtype)
+        grad_out = grad_out.contiguous()
+        gv = torch.empty_like(value)
+        gl = torch.empty_like(loc)
+        ga = torch.empty_like(attn)
+        if _aligned16(value, grad_out, gv):
+            need = _workspace_for(value.dtype, ctx.accum, dims)
+        else:
+            need = workspace_size(value.dtype, ctx.accum, dims, False)
+        ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=value.device) if need else None
+        dev = value.device
+        with torch.cuda.device(dev):
+            _lib.check(_lib.lib().msda_backward(
+                DTYPE_CODE[value.dtype], ACCUM[ctx.accum], 0, *dims, _ptr(value), _ptr(ss), _ptr(lsi), _ptr(loc),
+                _ptr(attn), _ptr(grad_out), _ptr(gv), _ptr(gl), _ptr(ga), _ptr(ws), need, _stream(dev)))
         return gv, None, None, gl, ga, None
 
 

@@ -123,11 +123,17 @@ struct TraceScope {
     }
 };
 
+int ilog2_floor(int v) {
+    int r = 0;
+    while (v > 1) v >>= 1, ++r;
+    return r;
+}
+
 // ---- tuning overrides (sweeps and tests), read once per process ----
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
 // params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
-// merge, nomerge.  None of them changes results beyond the rounding order of the
-// grad_value sums.
+// merge, nomerge, tiled, notiled, tp=<rows>.  None of them changes results
+// beyond the rounding order of the grad_value sums.
 
 struct Tune {
     int C = 0, P = 0, params = -1;
@@ -138,6 +144,8 @@ struct Tune {
     bool pdl = true;       // forward and zero kernel as programmatic dependents (off: nopdl)
     bool spec = false;     // the specialised forward even where the generic one is faster
     int merge = -1;        // backward corner merge: -1 by density, 0 off (nomerge), 1 on (merge)
+    int tiled = 0;         // FP32 accumulator on chip: 0 off (notiled, the default), 1 where the shape allows (tiled)
+    int lg_tp = 0;         // rows per tile of the on-chip accumulator (tp=<power of two>; 0: by D)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -160,6 +168,9 @@ const Tune& tune() {
             else if (!strcmp(tok, "spec")) r.spec = true;
             else if (!strcmp(tok, "merge")) r.merge = 1;
             else if (!strcmp(tok, "nomerge")) r.merge = 0;
+            else if (!strcmp(tok, "tiled")) r.tiled = 1;
+            else if (!strcmp(tok, "notiled")) r.tiled = 0;
+            else if (!strncmp(tok, "tp=", 3)) r.lg_tp = ilog2_floor(atoi(tok + 3));
         }
         return r;
     }();
@@ -216,6 +227,58 @@ msda_status check_ptr(const void* p, bool needed, size_t align, const char* name
     if (!p) return fail(MSDA_ERR_INVALID_ARG, "%s is NULL", name);
     if (!aligned(p, align)) return fail(MSDA_ERR_MISALIGNED, "%s is not aligned to %zu bytes", name, align);
     return MSDA_OK;
+}
+
+// ---- the FP32 accumulator on chip (msda_tiled.cuh) ----
+
+// Layout of the on-chip FP32 accumulator's passes for a problem: rows per
+// tile, tile counts, and its workspace (tile counters, offsets, cursors and
+// the entry array, each 16-byte aligned).
+struct TileLayout {
+    int lg_tp = 0;
+    int64_t tiles = 0, n_tiles = 0, n_entries = 0;
+    size_t off_counts = 0, off_offsets = 0, off_cursor = 0, off_entries = 0, bytes = 0;
+};
+
+// Whether a backward with the FP32 accumulator takes the on-chip path, by its
+// sizes alone (pointer alignment is checked at the call): 16-bit I/O, rows of
+// 2..6 16-byte vectors of 8 channels (D = 32, 64 or 96), 32-bit offsets inside a
+// batch image, fewer than 2^28 sampling points, sparse samples, the unfused
+// operator -- and only when asked for (MSDA_TUNE=tiled).  Measured on GB300
+// it is slower than the fp32 workspace in memory (encoder-scale stress
+// backward 11.0 ms against 6.9 ms; decoder 152 us against 56 us): the
+// accumulate pass is bound by the shared-memory atomic pipe (scalar fp32
+// atomics, L1/shared throughput at 69% of peak), which does fewer channel
+// additions per second than the L2 does with its 16-byte vector reductions,
+// and the count and place passes wait on the counters of the coarse levels'
+// few tiles.  Its workspace is ~26x smaller (329 MB against 8.56 GB there).
+bool tiled_layout(msda_dtype dt, msda_accum acc, const Dims& d, bool fused, TileLayout* tl) {
+    const Tune& t = tune();
+    if (t.tiled != 1 || fused || acc != MSDA_ACCUM_FP32 || (dt != MSDA_F16 && dt != MSDA_BF16)) return false;
+    if (d.D != 32 && d.D != 64 && d.D != 96) return false;
+    if (d.units <= 0 || d.n_value <= 0 || d.S * d.M * d.D > (1ll << 30)) return false;
+    const int64_t n_samples = d.units * d.L * d.K;
+    if (n_samples >= (1ll << 28)) return false;
+    // rows per tile: 64 KB of fp32 sums (512 rows of D = 32)
+    int lg = t.lg_tp > 0 ? t.lg_tp : ilog2_floor((int)(16384 / d.D));
+    if (lg < 4) lg = 4;
+    if (lg > 12) lg = 12;
+    const int64_t tiles = (d.S + (1ll << lg) - 1) >> lg;
+    const int64_t n_tiles = d.B * tiles * d.M;
+    if (n_tiles >= (1ll << 31) - 1) return false;
+    TileLayout r;
+    r.lg_tp = lg;
+    r.tiles = tiles;
+    r.n_tiles = n_tiles;
+    r.n_entries = 4 * n_samples;   // a point touches at most four tiles
+    auto up16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
+    r.off_counts = 0;
+    r.off_offsets = up16(r.off_counts + (size_t)n_tiles * 4);
+    r.off_cursor = up16(r.off_offsets + (size_t)(n_tiles + 1) * 4);
+    r.off_entries = up16(r.off_cursor + (size_t)n_tiles * 4);
+    r.bytes = up16(r.off_entries + (size_t)r.n_entries * 4);
+    *tl = r;
+    return true;
 }
 
 // ---- launch planning ----
@@ -614,6 +677,10 @@ const char* msda_kernel_name(int k) {
     case MSDA_KERNEL_BACKWARD: return "backward";
     case MSDA_KERNEL_ZERO: return "zero";
     case MSDA_KERNEL_CONVERT: return "convert";
+    case MSDA_KERNEL_TILE_COUNT: return "tile_count";
+    case MSDA_KERNEL_TILE_SCAN: return "tile_scan";
+    case MSDA_KERNEL_TILE_PLACE: return "tile_place";
+    case MSDA_KERNEL_TILE_ACCUM: return "tile_accum";
     }
     return "unknown";
 }
@@ -770,7 +837,11 @@ size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, i
         return (size_t)(n + msda::kDetHeaderBytes);
     }
     if (dt != MSDA_F16 && dt != MSDA_BF16) return 0;
-    if (msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q) != MSDA_ACCUM_FP32) return 0;
+    const msda_accum acc = msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q);
+    if (acc != MSDA_ACCUM_FP32) return 0;
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    TileLayout tl;
+    if (L >= 0 && K >= 0 && check_dims(dt, d) == MSDA_OK && tiled_layout(dt, acc, d, false, &tl)) return tl.bytes;
     int64_t n;
     if (!mul_ok(B, S, &n) || !mul_ok(n, M, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 4, &n)) return SIZE_MAX;
     return (size_t)n;
@@ -779,6 +850,113 @@ size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, i
 }  // extern "C"
 
 namespace {
+
+// Backward with the FP32 accumulator on chip (msda_tiled.cuh): the gather
+// kernel without its scatter (grad_sampling_locations, grad_attention_weights),
+// then count, scan, place and accumulate for grad_value.  Nothing is enqueued
+// unless the workspace and the plan pass.
+msda_status backward_tiled(msda_dtype dt, bool accumulate, const Dims& d, const TileLayout& tl, const void* value,
+                           const int64_t* shapes, const int64_t* starts, const void* loc, const void* attn,
+                           const void* grad_out, void* grad_value, void* grad_loc, void* grad_attn, void* workspace,
+                           size_t workspace_bytes, cudaStream_t st) {
+    if (!workspace || workspace_bytes < tl.bytes)
+        return fail(MSDA_ERR_WORKSPACE,
+                    "FP32 accumulation needs a %zu-byte workspace (got %zu at %p; with 16-byte aligned value, "
+                    "grad_out and grad_value)", tl.bytes, workspace_bytes, workspace);
+    if (!aligned(workspace, 16)) return fail(MSDA_ERR_WORKSPACE, "workspace is not 16-byte aligned");
+    msda_status s;
+    DeviceInfo* di = nullptr;
+    if ((s = device_info(&di))) return s;
+    KernelArgs a{};
+    Plan pl{};
+    if ((s = make_plan(dt, d, true, di->sms, true, loc, attn, pl, a, false))) return s;
+    if (!pl.spec) return fail(MSDA_ERR_UNSUPPORTED, "on-chip FP32 accumulation needs the specialised kernels");
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    msda::TileArgs t{};
+    t.loc = loc;
+    t.attn = attn;
+    t.grad_out = grad_out;
+    t.grad_value = grad_value;
+    t.shapes = shapes;
+    t.starts = starts;
+    t.err = di->err;
+    t.counts = reinterpret_cast<unsigned*>(ws + tl.off_counts);
+    t.offsets = reinterpret_cast<unsigned*>(ws + tl.off_offsets);
+    t.cursor = reinterpret_cast<unsigned*>(ws + tl.off_cursor);
+    t.entries = reinterpret_cast<unsigned*>(ws + tl.off_entries);
+    t.S = d.S;
+    t.M = (int)d.M;
+    t.D = (int)d.D;
+    t.L = (int)d.L;
+    t.K = (int)d.K;
+    t.LK = (int)(d.L * d.K);
+    t.Q = (int)d.Q;
+    t.n_samples = (int)(d.units * d.L * d.K);
+    t.div_lk = fast_div((uint32_t)(d.L * d.K));
+    t.div_k = fast_div((uint32_t)d.K);
+    t.div_qm = fast_div((uint32_t)(d.Q * d.M));
+    t.div_m = fast_div((uint32_t)d.M);
+    t.lg_tp = tl.lg_tp;
+    t.tiles = (int)tl.tiles;
+    t.n_tiles = (int)tl.n_tiles;
+    t.accumulate = accumulate ? 1 : 0;
+
+    // gather: grad_sampling_locations, grad_attention_weights
+    a.value = value;
+    a.shapes = shapes;
+    a.starts = starts;
+    a.loc = loc;
+    a.attn = attn;
+    a.grad_out = grad_out;
+    a.grad_acc = nullptr;
+    a.grad_loc = grad_loc;
+    a.grad_attn = grad_attn;
+    a.err = di->err;
+    pl.pdl = false;
+    auto launched = [&](const char* what) -> msda_status {
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? MSDA_OK : cuda_fail(e, what);
+    };
+    {
+        TraceScope ts(st);
+        switch (dt) {
+        case MSDA_F16: msda::launch_backward_gather<__half>(a, pl, st); break;
+        default: msda::launch_backward_gather<__nv_bfloat16>(a, pl, st); break;
+        }
+        ts.end(MSDA_KERNEL_BACKWARD, d.units);
+        if ((s = launched("backward gather kernel launch"))) return s;
+    }
+    if ((s = launch_zero(t.counts, tl.n_tiles * 4, di->sms, st))) return s;
+    {
+        TraceScope ts(st);
+        if (dt == MSDA_F16) msda::launch_tile_count<__half>(t, st);
+        else msda::launch_tile_count<__nv_bfloat16>(t, st);
+        ts.end(MSDA_KERNEL_TILE_COUNT, t.n_samples);
+        if ((s = launched("tile count kernel launch"))) return s;
+    }
+    {
+        TraceScope ts(st);
+        if (dt == MSDA_F16) msda::launch_tile_scan<__half>(t, st);
+        else msda::launch_tile_scan<__nv_bfloat16>(t, st);
+        ts.end(MSDA_KERNEL_TILE_SCAN, t.n_tiles);
+        if ((s = launched("tile scan kernel launch"))) return s;
+    }
+    {
+        TraceScope ts(st);
+        if (dt == MSDA_F16) msda::launch_tile_place<__half>(t, st);
+        else msda::launch_tile_place<__nv_bfloat16>(t, st);
+        ts.end(MSDA_KERNEL_TILE_PLACE, t.n_samples);
+        if ((s = launched("tile place kernel launch"))) return s;
+    }
+    {
+        TraceScope ts(st);
+        if (dt == MSDA_F16) msda::launch_tile_accum<__half>(t, pl.nv, st);
+        else msda::launch_tile_accum<__nv_bfloat16>(t, pl.nv, st);
+        ts.end(MSDA_KERNEL_TILE_ACCUM, t.n_tiles);
+        if ((s = launched("tile accumulate kernel launch"))) return s;
+    }
+    return MSDA_OK;
+}
 
 // Backward after argument validation; `fz` non-NULL selects the fused
 // operator (sampling_locations / attention_weights then hold offsets /
@@ -798,6 +976,15 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
                                       attention_weights, grad_out, grad_value, grad_sampling_locations,
                                       grad_attention_weights, workspace, workspace_bytes, st, fz);
     const bool use_ws = dt != MSDA_F32 && acc == MSDA_ACCUM_FP32 && work && d.n_value > 0;
+    TileLayout tl;
+    if (use_ws && tiled_layout(dt, acc, d, fz != nullptr, &tl)) {
+        const bool aligned16 = aligned(value, 16) && aligned(grad_out, 16) && aligned(grad_value, 16);
+        if (aligned16)
+            return backward_tiled(dt, accumulate, d, tl, value, spatial_shapes, level_start_index, sampling_locations,
+                                  attention_weights, grad_out, grad_value, grad_sampling_locations,
+                                  grad_attention_weights, workspace, workspace_bytes, st);
+        // unaligned pointers: the workspace path below, with its B*S*M*D*4 bytes
+    }
     if (use_ws) {
         const size_t need = (size_t)d.n_value * 4;
         if (!workspace || workspace_bytes < need)

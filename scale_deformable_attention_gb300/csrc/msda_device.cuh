@@ -970,9 +970,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
 // zero kernel, griddepcontrol.wait before the first scatter lets the gather
 // phase of the first round overlap the zeroing of grad_value; launched
 // normally, the wait returns at once.
-// MERGE: 0 none, kMergeCells whole cells only, kMergeCorners every shared corner.
+// MERGE: 0 none, kMergeCells whole cells only, kMergeCorners every shared corner;
+// kGatherOnly: no scatter at all (grad_attn / grad_loc only; grad_value is
+// accumulated on chip by the tiled passes of msda_tiled.cuh).
 constexpr int kMergeCells = 1;
 constexpr int kMergeCorners = 2;
+constexpr int kGatherOnly = -1;
 
 template <typename T, typename ACC, int NV, bool FUSED, int MERGE>
 __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
@@ -1142,124 +1145,126 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
             }
         }
 
-        // Corner merge (MERGE).  Samples of the point group that add some of
-        // the same rows merge first: each shared row is added once, by the
-        // last sample holding it, with the sum of their coefficients
-        // A * w_k, and the others skip that corner.  A corner merges only
-        // when it is inside the level for both samples, so equal offsets mean
-        // the same row.  Whole cells: samples with the same cell offset and
-        // level width (an equivalence, so every holder is found).  Every
-        // shared corner: also cells that touch, by edge or corner, on a level
-        // at least three pixels wide.  Two cells sharing a corner row are
-        // within one pixel of each other, and for W >= 3 the nine such offsets
-        // are distinct, so every pair holding a row is found (a missed pair
-        // could lose a coefficient: an intermediate sample would absorb it and
-        // then skip the row for a later holder that did not).
-        // The reductions bound this kernel when samples cluster.  Measured on
-        // GB300, encoder backward: native 346 -> 281 us with whole cells
-        // (17% fewer reductions; 306 us with every corner, whose extra
-        // instructions cost more than its extra 12%); fp32 workspace
-        // 601 -> 454 us with every corner (479 with whole cells).  With
-        // uniformly spread samples (decoder) nothing merges and the code
-        // costs ~2 us, so it is compiled only into the merging kernels.
-        float mc[4];
-        unsigned smask = me.mask;
-        {
-            float w0[4];
-            corner_weights(me.lx, me.ly, w0);
-            float oc[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mc[k] = oc[k] = wa * w0[k];
-#pragma unroll
-            for (int jj = 0; jj < kC; ++jj) {
-                if constexpr (MERGE == 0) break;
-                const int src = team_lane(ln, jj, ln.p);
-                const int o2 = __shfl_sync(0xffffffffu, me.o, src);
-                const int w2 = __shfl_sync(0xffffffffu, me.wmd, src);
-                const unsigned m2 = __shfl_sync(0xffffffffu, me.mask, src);
-                float c2[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) c2[k] = __shfl_sync(0xffffffffu, oc[k], src);
-                if (jj == ln.c || w2 != me.wmd) continue;
-                const bool earlier = jj < ln.c;
-                // my corner k is the other sample's corner k2
-                auto share = [&](int k, int k2) {
-                    if (((me.mask >> k) & 1u) && ((m2 >> k2) & 1u)) {
-                        if (earlier) mc[k] += c2[k2];
-                        else smask &= ~(1u << k);
-                    }
-                };
-                const int dd = o2 - me.o;  // the other cell relative to mine
-                if constexpr (MERGE == kMergeCells) {
-                    if (dd == 0) {
-                        share(0, 0); share(1, 1); share(2, 2); share(3, 3);
-                    }
-                } else {
-                    if (me.wmd < 3 * MD) continue;
-                    if (dd == 0) {
-                        share(0, 0); share(1, 1); share(2, 2); share(3, 3);
-                    } else if (dd == MD) {                  // one pixel right
-                        share(1, 0); share(3, 2);
-                    } else if (dd == -MD) {                 // one pixel left
-                        share(0, 1); share(2, 3);
-                    } else if (dd == me.wmd) {              // one row down
-                        share(2, 0); share(3, 1);
-                    } else if (dd == -me.wmd) {             // one row up
-                        share(0, 2); share(1, 3);
-                    } else if (dd == me.wmd + MD) {         // down-right
-                        share(3, 0);
-                    } else if (dd == me.wmd - MD) {         // down-left
-                        share(2, 1);
-                    } else if (dd == MD - me.wmd) {         // up-right
-                        share(1, 2);
-                    } else if (dd == -MD - me.wmd) {        // up-left
-                        share(0, 3);
+        if constexpr (MERGE >= 0) {
+            // Corner merge (MERGE).  Samples of the point group that add some of
+            // the same rows merge first: each shared row is added once, by the
+            // last sample holding it, with the sum of their coefficients
+            // A * w_k, and the others skip that corner.  A corner merges only
+            // when it is inside the level for both samples, so equal offsets mean
+            // the same row.  Whole cells: samples with the same cell offset and
+            // level width (an equivalence, so every holder is found).  Every
+            // shared corner: also cells that touch, by edge or corner, on a level
+            // at least three pixels wide.  Two cells sharing a corner row are
+            // within one pixel of each other, and for W >= 3 the nine such offsets
+            // are distinct, so every pair holding a row is found (a missed pair
+            // could lose a coefficient: an intermediate sample would absorb it and
+            // then skip the row for a later holder that did not).
+            // The reductions bound this kernel when samples cluster.  Measured on
+            // GB300, encoder backward: native 346 -> 281 us with whole cells
+            // (17% fewer reductions; 306 us with every corner, whose extra
+            // instructions cost more than its extra 12%); fp32 workspace
+            // 601 -> 454 us with every corner (479 with whole cells).  With
+            // uniformly spread samples (decoder) nothing merges and the code
+            // costs ~2 us, so it is compiled only into the merging kernels.
+            float mc[4];
+            unsigned smask = me.mask;
+            {
+                float w0[4];
+                corner_weights(me.lx, me.ly, w0);
+                float oc[4];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) mc[k] = oc[k] = wa * w0[k];
+    #pragma unroll
+                for (int jj = 0; jj < kC; ++jj) {
+                    if constexpr (MERGE == 0) break;
+                    const int src = team_lane(ln, jj, ln.p);
+                    const int o2 = __shfl_sync(0xffffffffu, me.o, src);
+                    const int w2 = __shfl_sync(0xffffffffu, me.wmd, src);
+                    const unsigned m2 = __shfl_sync(0xffffffffu, me.mask, src);
+                    float c2[4];
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) c2[k] = __shfl_sync(0xffffffffu, oc[k], src);
+                    if (jj == ln.c || w2 != me.wmd) continue;
+                    const bool earlier = jj < ln.c;
+                    // my corner k is the other sample's corner k2
+                    auto share = [&](int k, int k2) {
+                        if (((me.mask >> k) & 1u) && ((m2 >> k2) & 1u)) {
+                            if (earlier) mc[k] += c2[k2];
+                            else smask &= ~(1u << k);
+                        }
+                    };
+                    const int dd = o2 - me.o;  // the other cell relative to mine
+                    if constexpr (MERGE == kMergeCells) {
+                        if (dd == 0) {
+                            share(0, 0); share(1, 1); share(2, 2); share(3, 3);
+                        }
+                    } else {
+                        if (me.wmd < 3 * MD) continue;
+                        if (dd == 0) {
+                            share(0, 0); share(1, 1); share(2, 2); share(3, 3);
+                        } else if (dd == MD) {                  // one pixel right
+                            share(1, 0); share(3, 2);
+                        } else if (dd == -MD) {                 // one pixel left
+                            share(0, 1); share(2, 3);
+                        } else if (dd == me.wmd) {              // one row down
+                            share(2, 0); share(3, 1);
+                        } else if (dd == -me.wmd) {             // one row up
+                            share(0, 2); share(1, 3);
+                        } else if (dd == me.wmd + MD) {         // down-right
+                            share(3, 0);
+                        } else if (dd == me.wmd - MD) {         // down-left
+                            share(2, 1);
+                        } else if (dd == MD - me.wmd) {         // up-right
+                            share(1, 2);
+                        } else if (dd == -MD - me.wmd) {        // up-left
+                            share(0, 3);
+                        }
                     }
                 }
             }
-        }
 
-        // scatter: A * w_corner * g into the inside corners
-        if (!waited) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            waited = true;
-            if constexpr (std::is_same<ACC, long long>::value) dscale = det_scale(a.det, (long long)a.Q * a.LK);
-        }
-#pragma unroll
-        for (int j = 0; j < kC; ++j) {
-            const int src = team_lane(ln, j, ln.p);
-            const int so = __shfl_sync(0xffffffffu, me.o, src);
-            const int swmd = __shfl_sync(0xffffffffu, me.wmd, src);
-            const unsigned smk = __shfl_sync(0xffffffffu, smask, src);
-            float cj[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) cj[k] = __shfl_sync(0xffffffffu, mc[k], src);
-            const int off[4] = {so, so + MD, so + swmd, so + swmd + MD};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (!((smk >> k) & 1u)) continue;
-                const float2 cf = make_float2(cj[k], cj[k]);
-#pragma unroll
-                for (int n = 0; n < NV; ++n) {
-                    if constexpr (ILV) {
-                        // each contribution times 2^F (exact), rounded once to an integer
-                        long long* q = ibase + off[k] + n * kC * EPV;
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) red_s64(q + kC * e, __float2ll_rn(cf.x * gi[n][e] * dscale));
-                    } else {
-                        float t[EPV];
-#pragma unroll
-                        for (int e = 0; e < EPV; e += 2) {
-                            const float2 r = __fmul2_rn(cf, make_float2(g[n][e], g[n][e + 1]));
-                            t[e] = r.x;
-                            t[e + 1] = r.y;
-                        }
-                        if constexpr (SPLIT) {
-                            float* q = gbase + off[k] + n * kC * EPV;
-                            red_v4_f32(q, t[0], t[1], t[2], t[3]);
-                            red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+            // scatter: A * w_corner * g into the inside corners
+            if (!waited) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                waited = true;
+                if constexpr (std::is_same<ACC, long long>::value) dscale = det_scale(a.det, (long long)a.Q * a.LK);
+            }
+    #pragma unroll
+            for (int j = 0; j < kC; ++j) {
+                const int src = team_lane(ln, j, ln.p);
+                const int so = __shfl_sync(0xffffffffu, me.o, src);
+                const int swmd = __shfl_sync(0xffffffffu, me.wmd, src);
+                const unsigned smk = __shfl_sync(0xffffffffu, smask, src);
+                float cj[4];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) cj[k] = __shfl_sync(0xffffffffu, mc[k], src);
+                const int off[4] = {so, so + MD, so + swmd, so + swmd + MD};
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (!((smk >> k) & 1u)) continue;
+                    const float2 cf = make_float2(cj[k], cj[k]);
+    #pragma unroll
+                    for (int n = 0; n < NV; ++n) {
+                        if constexpr (ILV) {
+                            // each contribution times 2^F (exact), rounded once to an integer
+                            long long* q = ibase + off[k] + n * kC * EPV;
+    #pragma unroll
+                            for (int e = 0; e < EPV; ++e) red_s64(q + kC * e, __float2ll_rn(cf.x * gi[n][e] * dscale));
                         } else {
-                            Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                            float t[EPV];
+    #pragma unroll
+                            for (int e = 0; e < EPV; e += 2) {
+                                const float2 r = __fmul2_rn(cf, make_float2(g[n][e], g[n][e + 1]));
+                                t[e] = r.x;
+                                t[e + 1] = r.y;
+                            }
+                            if constexpr (SPLIT) {
+                                float* q = gbase + off[k] + n * kC * EPV;
+                                red_v4_f32(q, t[0], t[1], t[2], t[3]);
+                                red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+                            } else {
+                                Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
+                            }
                         }
                     }
                 }

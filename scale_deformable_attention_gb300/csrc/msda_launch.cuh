@@ -5,6 +5,7 @@
 #pragma once
 
 #include "msda_device.cuh"
+#include "msda_tiled.cuh"
 
 namespace msda {
 
@@ -183,6 +184,50 @@ void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st
     msda_widen_kernel<T><<<grid, kBlockThreads, 0, st>>>(gv, ws, n);
 }
 
+// ---- the on-chip FP32 accumulator (msda_tiled.cuh) ----
+
+// The backward's gather phase alone: grad_sampling_locations and
+// grad_attention_weights, no grad_value scatter (specialised plans only).
+template <typename T>
+void launch_backward_gather(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
+    MSDA_DISPATCH_NV3(pl.nv, (launch_plan(msda_bwd4_kernel<T, T, NV, false, kGatherOnly>, a, pl, st)))
+}
+
+template <typename T>
+void launch_tile_count(const TileArgs& t, cudaStream_t st) {
+    const unsigned grid = (unsigned)((t.n_samples + kBlockThreads - 1) / kBlockThreads);
+    msda_tile_count_kernel<T><<<grid, kBlockThreads, 0, st>>>(t);
+}
+
+template <typename T>
+void launch_tile_place(const TileArgs& t, cudaStream_t st) {
+    const unsigned grid = (unsigned)((t.n_samples + kBlockThreads - 1) / kBlockThreads);
+    msda_tile_place_kernel<T><<<grid, kBlockThreads, 0, st>>>(t);
+}
+
+template <typename T>
+void launch_tile_scan(const TileArgs& t, cudaStream_t st) {
+    msda_tile_scan_kernel<T><<<1, kScanThreads, 0, st>>>(t);
+}
+
+// Shared memory of the accumulate pass: (1 << lg_tp) rows of D fp32.
+inline size_t tile_smem(int lg_tp, int D) { return ((size_t)1 << lg_tp) * (size_t)D * sizeof(float); }
+
+template <typename T, int NV>
+static void tile_accum_go(const TileArgs& t, cudaStream_t st) {
+    const size_t smem = tile_smem(t.lg_tp, t.D);
+    // the static level table comes on top of the dynamic rows: allow the
+    // dynamic size explicitly whenever the two together pass the default 48 KB
+    if (smem + sizeof(Level) * MSDA_MAX_LEVELS > 48 * 1024)
+        cudaFuncSetAttribute(msda_tile_accum_kernel<T, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    msda_tile_accum_kernel<T, NV><<<(unsigned)t.n_tiles, kBlockThreads, smem, st>>>(t);
+}
+
+template <typename T>
+void launch_tile_accum(const TileArgs& t, int nv, cudaStream_t st) {
+    MSDA_DISPATCH_NV3(nv, (tile_accum_go<T, NV>(t, st)))
+}
+
 #ifndef MSDA_INSTANTIATE
 // defined in msda_kernels_<dtype>.cu
 #define MSDA_EXTERN_IO(T)                                                                  \
@@ -207,6 +252,16 @@ MSDA_EXTERN_IO(__nv_bfloat16)
 MSDA_EXTERN_HALF(__half)
 MSDA_EXTERN_HALF(__nv_bfloat16)
 #undef MSDA_EXTERN_HALF
+#define MSDA_EXTERN_TILED(T)                                                                     \
+    extern template void launch_backward_gather<T>(const KernelArgs&, const Plan&, cudaStream_t); \
+    extern template void launch_tile_count<T>(const TileArgs&, cudaStream_t);                    \
+    extern template void launch_tile_place<T>(const TileArgs&, cudaStream_t);                    \
+    extern template void launch_tile_scan<T>(const TileArgs&, cudaStream_t);                     \
+    extern template void launch_tile_accum<T>(const TileArgs&, int, cudaStream_t);
+MSDA_EXTERN_TILED(float)
+MSDA_EXTERN_TILED(__half)
+MSDA_EXTERN_TILED(__nv_bfloat16)
+#undef MSDA_EXTERN_TILED
 #endif
 
 }  // namespace msda

@@ -94,6 +94,10 @@ CASES = [
     ("oddD_fp32", (), "auto"),
     ("oddD_fp32", (("dtype", "bf16"), ("B", 2)), "fp32"),
     ("stress_bf16", (("B", 1), ("Q", 3000), ("shapes", ((96, 128), (48, 64), (24, 32), (12, 16)))), "fp32"),
+    # sparse samples, wider rows (two and three 16-byte vectors per lane) with the FP32 accumulator
+    ("stress_bf16", (("B", 2), ("Q", 2000), ("shapes", ((96, 128), (48, 64), (24, 32), (12, 16)))), "fp32"),
+    ("decoder_bf16", (("dtype", "f16"), ("D", 64), ("B", 2)), "fp32"),
+    ("decoder_bf16", (("D", 96), ("B", 1), ("Q", 77)), "fp32"),
 ]
 
 

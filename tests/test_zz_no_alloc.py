@@ -121,45 +121,43 @@ def test_static_workspace_accumulates(lib):
     assert rel_l2(f64(gv), f64(ref)) <= TOL["bf16"]
 
 
-def _single_level(S, M, D, Q, seed):
-    """One level of 1 x S pixels (or 512 x 512), bf16, uniform locations."""
-    shapes = ((512, S // 512),) if S % 512 == 0 else ((1, S),)
-    return W.Workload("boundary", B=1, M=M, D=D, K=1, shapes=shapes, Q=Q, dtype="bf16", loc="uniform01",
-                      logits="uniform01", seed=seed)
-
-
 def test_static_workspace_size_boundary(lib):
     """A call whose scratch is exactly the array's size is accepted and
     correct; one element more is rejected with MSDA_ERR_WORKSPACE before
-    anything is enqueued (grad_value keeps its contents)."""
+    anything is enqueued (the outputs keep their contents).  One channel per
+    head (D = 1) takes the FP32 accumulator with an fp32 mirror of grad_value,
+    B*S*M*D*4 bytes."""
     import scale_deformable_attention_gb300 as msda
 
     f = _entry(lib)
-    # accepted at the boundary: 32 MiB of bf16 value, an fp32 scratch of exactly LIMIT bytes
-    M, D, Q = 1, 64, 64
-    S = LIMIT // 4 // (M * D)
-    wl = _single_level(S, M, D, Q, seed=24)
+    # accepted at the boundary: 2^24 rows of one bf16 channel (32 MiB of value), 64 MiB of fp32 scratch
+    side = 4096
+    wl = W.Workload("boundary", B=1, M=1, D=1, K=2, shapes=((side, side),), Q=300, dtype="bf16", loc="uniform01",
+                    logits="uniform01", seed=24)
     dims = (wl.B, wl.S, wl.M, wl.D, wl.L, wl.K, wl.Qn)
-    need = _need(lib, "bf16", dims)
-    assert 0 < need <= LIMIT
+    assert _need(lib, "bf16", dims) == LIMIT
     inp = W.make_inputs(wl)
     t = W.to_torch(inp, "bf16", DEV)
     gv = torch.full_like(t["value"], 3.0)
     gl = torch.empty_like(t["sampling_locations"])
     ga = torch.empty_like(t["attention_weights"])
     assert _call(f, "bf16", 0, dims, t, gv, gl, ga) == 0, lib.msda_last_error()
-    ref_gv, ref_gl, ref_ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"],
-                                           t["sampling_locations"], t["attention_weights"], t["grad_out"],
-                                           accum="fp32")
+    torch.cuda.synchronize()
+    o_gv, o_gl, o_ga = oracle.backward(inp, "bf16")
+    for got, want, name in ((gv, o_gv, "grad_value"), (gl, o_gl, "grad_loc"), (ga, o_ga, "grad_attn")):
+        e = rel_l2(f64(got), want)
+        assert e <= TOL["bf16"], f"at the size limit, {name} vs oracle: rel-L2 {e:.3e}"
+    ref_gv, _, _ = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                                 t["attention_weights"], t["grad_out"], accum="fp32")
     torch.cuda.synchronize()
     assert rel_l2(f64(gv), f64(ref_gv)) <= TOL["bf16"]
-    assert torch.equal(gl, ref_gl) and torch.equal(ga, ref_ga)
+    del t, gv, gl, ga, inp, ref_gv
 
-    # rejected one element above: the smallest S whose scratch exceeds the array
+    # rejected one element above
     M, D, Q = 1, 1, 1
     S = LIMIT // 4 + 1
     dims = (1, S, M, D, 1, 1, Q)
-    assert _need(lib, "bf16", dims) > LIMIT
+    assert _need(lib, "bf16", dims) == LIMIT + 4
     value = torch.zeros((1, S, M, D), dtype=torch.bfloat16, device=DEV)
     z = {"value": value, "spatial_shapes": torch.tensor([[1, S]], dtype=torch.int64, device=DEV),
          "level_start_index": torch.zeros(1, dtype=torch.int64, device=DEV),
