@@ -338,12 +338,12 @@ def job_throughput(units_per_rank: int, world: int, steps: int, total_ms: float)
 
 def unique_fractions(model: dict, kernels: dict, peak: float):
     """Compulsory-byte (unique value rows) fractions of the measured peak for
-    the traced forward and backward (zero + kernel + convert) durations."""
+    the traced forward and backward (every other kernel of the step: zero,
+    backward passes, convert) durations per step."""
     if "forward_unique" not in model or "forward" not in kernels or "backward" not in kernels:
         return None
-    tf = kernels["forward"]["avg_ms"]
-    tb = sum(kernels[k]["avg_ms"] * kernels[k]["launches"] / kernels["backward"]["launches"]
-             for k in ("zero", "backward", "convert") if k in kernels)
+    tf = kernels["forward"]["ms_per_step"]
+    tb = sum(v["ms_per_step"] for k, v in kernels.items() if k != "forward")
     return {"unique_rows": model["unique_rows"], "forward_bytes": model["forward_unique"],
             "backward_bytes": model["bwd_total_unique"],
             "forward_frac": round(model["forward_unique"] / (tf / 1e3) / 1e9 / peak, 4),
@@ -351,18 +351,30 @@ def unique_fractions(model: dict, kernels: dict, peak: float):
             "peak": peak, "unit": "GB/s"}
 
 
-def reduction_ceiling_for(accum: str, dtype: str):
+def reduction_row_bytes(wl: W.Workload, accum: str) -> int:
+    """Bytes of one corner row as the backward reduces it (D channels at the
+    accumulator's width), rounded up to the probe's sizes (16 .. 512)."""
+    es_acc = W.ESIZE[wl.dtype] if accum == "native" else 4
+    rb = 16
+    while rb < min(512, wl.D * es_acc):
+        rb *= 2
+    return rb
+
+
+def reduction_ceiling_for(wl: W.Workload, accum: str):
     """32-byte reduction sectors per second the L2 takes for this backward's
-    kind of reduction (msda_reduction_ceiling), or None (the deterministic
-    accumulator's scalar integer reductions are another pattern)."""
+    kind of reduction (msda_reduction_ceiling: whole corner rows, 16-byte
+    reductions from adjacent lanes), or None (the deterministic accumulator's
+    scalar integer reductions are another pattern)."""
     import torch
 
     import scale_deformable_attention_gb300 as msda
 
     if accum == "deterministic":
         return None
-    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
-    return msda.reduction_ceiling(tdt if accum == "native" else torch.float32)
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[wl.dtype]
+    return msda.reduction_ceiling(tdt if accum == "native" else torch.float32,
+                                  row_bytes=reduction_row_bytes(wl, accum))
 
 
 def reduction_roofline(wl: W.Workload, corners: int, accum: str, kernels: dict, ceiling):
@@ -373,11 +385,12 @@ def reduction_roofline(wl: W.Workload, corners: int, accum: str, kernels: dict, 
         return None
     es_acc = W.ESIZE[wl.dtype] if accum == "native" else 4
     sectors = corners * ((wl.D * es_acc + 31) // 32)
-    achieved = sectors / (kernels["backward"]["avg_ms"] / 1e3)
+    achieved = sectors / (kernels["backward"]["ms_per_step"] / 1e3)
     return {"kernel": "backward", "bound": "l2_reductions", "sectors": sectors,
             "achieved_gsectors_s": round(achieved / 1e9, 2), "ceiling_gsectors_s": round(ceiling / 1e9, 2),
             "frac": round(achieved / ceiling, 4),
-            "ceiling_source": "msda_reduction_ceiling on this GPU (random sectors, two 16-byte reductions each)"}
+            "ceiling_source": f"msda_reduction_ceiling on this GPU (random {reduction_row_bytes(wl, accum)}-byte rows, "
+                              "16-byte reductions from adjacent lanes)"}
 
 
 def graph_cross_check(st, steps: int):
@@ -427,13 +440,16 @@ def bound_of(kernel: str, wl: W.Workload, accum: str, l2: int, tiled: bool = Fal
     return "l2_reductions" if kernel == "backward" and not tiled else "l2"
 
 
-def kernel_table(recs):
-    """Per-kernel launches, mean duration and share of a traced pass."""
+def kernel_table(recs, steps: int):
+    """Per-kernel launches, mean duration, time per step (a kernel may launch
+    more than once per step: the backward runs one pass per level on large
+    problems) and share of a traced pass of `steps` steps."""
     per = {}
     for name, ms, work in recs:
         per.setdefault(name, []).append(ms)
     tot = sum(sum(v) for v in per.values()) or 1.0
-    return per, {k: {"launches": len(v), "avg_ms": round(statistics.mean(v), 5), "share": round(sum(v) / tot, 4)}
+    return per, {k: {"launches": len(v), "avg_ms": round(statistics.mean(v), 5),
+                     "ms_per_step": round(sum(v) / steps, 5), "share": round(sum(v) / tot, 4)}
                  for k, v in per.items()}
 
 
@@ -450,20 +466,25 @@ def traced_pass(st, steps: int):
 
 
 def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2: int, kernels: dict):
+    """The dominant kernel against the measured HBM peak: its algorithmic
+    bytes per step (per-corner model) over its traced time per step, i.e. the
+    per-launch ratio when it launches once per step, and the launch-weighted
+    one when it launches once per level."""
     peak, peak_kind = peaks()
-    avg_ms = statistics.mean(per[dom])
+    k = kernels[dom]
     # the backward kernel without its scatter when the accumulate pass holds grad_value
     alg = model["backward_gather"] if dom == "backward" and "tile_accum" in per else model[dom]
-    achieved = alg / (avg_ms / 1e3) / 1e9
+    achieved = alg / (k["ms_per_step"] / 1e3) / 1e9
     roof = {"kernel": dom, "bound": bound_of(dom, wl, accum, l2, "tile_accum" in per), "achieved": round(achieved, 1),
-            "peak": peak,
-            "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": recorded_traffic(dom, wl.name, accum),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(dom, wl.name, accum),
             "algorithmic_bytes": alg, "bytes_model": "per-corner (every in-level corner row each time)",
-            "avg_launch_ms": round(avg_ms, 5), "peak_source": peak_kind, "launches_traced": len(per[dom])}
+            "avg_launch_ms": k["avg_ms"], "launches_per_step": round(k["launches"] / max(1, k.get("steps", 1)), 3),
+            "ms_per_step": k["ms_per_step"], "peak_source": peak_kind, "launches_traced": k["launches"]}
     uf = unique_fractions(model, kernels, peak)
     if uf:
-        roof["compulsory_frac"] = uf["backward_frac"] if dom in ("backward", "zero", "convert") else uf["forward_frac"]
-        roof["compulsory_scope"] = ("backward pass (zero + kernel + convert)" if dom != "forward"
+        roof["compulsory_frac"] = uf["backward_frac"] if dom != "forward" else uf["forward_frac"]
+        roof["compulsory_scope"] = ("backward pass (every kernel after the forward)" if dom != "forward"
                                     else "forward pass")
     return roof
 
@@ -486,7 +507,7 @@ def run_ours(args):
     resolved = st.resolved
     corners, urows = corner_counts(wl, inp)
     model = byte_model(wl, corners, urows)
-    red_ceiling = reduction_ceiling_for(resolved, wl.dtype)
+    red_ceiling = reduction_ceiling_for(wl, resolved)
     l2 = l2_bytes(device)
 
     for _ in range(max(args.warmup, 3)):
@@ -514,8 +535,11 @@ def run_ours(args):
     value = job_throughput(wl.units, world, args.steps, total_ms)
 
     # per-kernel durations from a separate traced pass
-    recs, dropped = traced_pass(st, max(4, min(args.steps, args.trace_steps)))
-    per, kernels = kernel_table(recs)
+    n_traced = max(4, min(args.steps, args.trace_steps))
+    recs, dropped = traced_pass(st, n_traced)
+    per, kernels = kernel_table(recs, n_traced)
+    for v in kernels.values():
+        v["steps"] = n_traced
     dom = max(per, key=lambda k: sum(per[k])) if per else None
     roof = roofline_of(dom, per, wl, model, resolved, l2, kernels) if dom else None
     peak, _ = peaks()
@@ -579,7 +603,7 @@ def config_entry(wl: W.Workload, inp, accum: str, device, n: int, l2: int):
     tb = statistics.median(st.timed(st.backward, n))
     ts = statistics.median(st.timed(st.step, n))
     recs, _ = traced_pass(st, 4)
-    per, kernels = kernel_table(recs)
+    per, kernels = kernel_table(recs, 4)
     dom = max(per, key=lambda k: sum(per[k])) if per else None
     e = {"accum": accum, "accum_resolved": st.resolved, "fwd_ms": round(tf, 4), "bwd_ms": round(tb, 4),
          "step_ms": round(ts, 4), "step_units_per_s": round(wl.units / (ts / 1e3), 1),

@@ -279,26 +279,28 @@ int msda_version(void);
 /*
  * Measurement utility (not part of the operator): the L2's throughput for
  * the backward's kind of reduction traffic on the current device.  The
- * backward adds every in-level corner row into grad_value with relaxed
- * 16-byte vector reductions, two adjacent lanes per 32-byte sector, at rows
- * scattered over the tensor (ch. 5, "Scatter needs atomics",
- * "sem=relaxed").  This runs that pattern alone: random 32-byte sectors of
- * `scratch`, each taken by two 16-byte reductions of `kind` (0 bf16x2,
- * 1 f16x2, 2 f32), with `blocks_per_sm` blocks of 256 threads per SM, and
- * reports 32-byte sectors per second in *sectors_per_second (best of
- * `repeats` launches of 256 reductions per thread, after one warm-up).
+ * backward adds every in-level corner row into grad_value (or its fp32
+ * workspace) with relaxed 16-byte vector reductions, the row's row_bytes
+ * taken by row_bytes / 16 adjacent lanes, at rows scattered over the tensor
+ * (ch. 5, "Scatter needs atomics", "sem=relaxed").  This runs that pattern
+ * alone: rows of `row_bytes` (16, 32, 64, 128, 256 or 512) at random places of
+ * `scratch`, each taken by row_bytes / 16 lanes with one 16-byte reduction of
+ * `kind` (0 bf16x2, 1 f16x2, 2 f32) each, with `blocks_per_sm` blocks of 256
+ * threads per SM, and reports 32-byte sectors per second in
+ * *sectors_per_second (best of `repeats` launches of 256 reductions per
+ * thread, after one warm-up).
  *
  * scratch: device buffer of scratch_bytes (>= 1 MiB, 16-byte aligned); its
  * contents are overwritten.  Keep it inside the L2 (e.g. 64 MiB) to measure
  * the L2's reduction rate rather than DRAM's.  Unlike the operator calls
  * this one synchronises `stream` (it times with CUDA events) and is meant
  * for roofline reporting, not for the hot path.  Errors: NULL or small or
- * misaligned scratch, kind outside 0..2, blocks_per_sm outside 1..16 or
- * repeats outside 1..100 -> MSDA_ERR_INVALID_ARG; a CUDA failure ->
- * MSDA_ERR_CUDA.
+ * misaligned scratch, kind outside 0..2, row_bytes not listed above,
+ * blocks_per_sm outside 1..16 or repeats outside 1..100 ->
+ * MSDA_ERR_INVALID_ARG; a CUDA failure -> MSDA_ERR_CUDA.
  */
-msda_status msda_reduction_ceiling(int kind, int blocks_per_sm, int repeats, void* scratch, size_t scratch_bytes,
-                                   double* sectors_per_second, msda_stream_t stream);
+msda_status msda_reduction_ceiling(int kind, int row_bytes, int blocks_per_sm, int repeats, void* scratch,
+                                   size_t scratch_bytes, double* sectors_per_second, msda_stream_t stream);
 
 /*
  * Kernel trace.  While enabled, every kernel the library launches is

@@ -409,18 +409,20 @@ def multi_scale_deformable_attention_fused(value, spatial_shapes, level_start_in
 REDUCTION_KIND = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 
-def reduction_ceiling(dtype=torch.bfloat16, *, blocks_per_sm: int = 8, repeats: int = 5, scratch_mib: int = 64,
-                      device=None) -> float:
+def reduction_ceiling(dtype=torch.bfloat16, *, row_bytes: int = 64, blocks_per_sm: int = 8, repeats: int = 5,
+                      scratch_mib: int = 64, device=None) -> float:
     """32-byte sectors per second the L2 takes for the backward's kind of
-    reduction traffic (C ABI ``msda_reduction_ceiling``): random sectors of a
-    ``scratch_mib`` MiB buffer, two 16-byte ``dtype`` vector reductions per
-    sector.  Synchronises the current stream; a measurement, not an operator."""
+    reduction traffic (C ABI ``msda_reduction_ceiling``): rows of ``row_bytes``
+    at random places of a ``scratch_mib`` MiB buffer, each row taken by
+    row_bytes / 16 lanes with one 16-byte ``dtype`` vector reduction each.
+    Synchronises the current stream; a measurement, not an operator."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     scratch = torch.empty(scratch_mib << 20, dtype=torch.uint8, device=device)
     out = ctypes.c_double(0.0)
     with torch.cuda.device(device):
-        _lib.check(_lib.lib().msda_reduction_ceiling(REDUCTION_KIND[dtype], blocks_per_sm, repeats, _ptr(scratch),
-                                                     scratch.numel(), ctypes.byref(out), _stream(device)))
+        _lib.check(_lib.lib().msda_reduction_ceiling(REDUCTION_KIND[dtype], row_bytes, blocks_per_sm, repeats,
+                                                     _ptr(scratch), scratch.numel(), ctypes.byref(out),
+                                                     _stream(device)))
     return out.value
 
 

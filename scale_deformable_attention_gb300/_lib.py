@@ -50,7 +50,7 @@ def _declare(lib):
     lib.msda_forward_fused.restype = c_int
     lib.msda_backward_fused.argtypes = [c_int, c_int, c_uint] + dims + [vp] * 11 + [vp, sz, vp]
     lib.msda_backward_fused.restype = c_int
-    lib.msda_reduction_ceiling.argtypes = [c_int, c_int, c_int, vp, sz, ctypes.POINTER(ctypes.c_double), vp]
+    lib.msda_reduction_ceiling.argtypes = [c_int, c_int, c_int, c_int, vp, sz, ctypes.POINTER(ctypes.c_double), vp]
     lib.msda_reduction_ceiling.restype = c_int
     lib.msda_backward_workspace_size.argtypes = [c_int, c_int] + dims
     lib.msda_backward_workspace_size.restype = sz

@@ -132,7 +132,7 @@ int ilog2_floor(int v) {
 // ---- tuning overrides (sweeps and tests), read once per process ----
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
 // params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
-// merge, nomerge, tiled, notiled, tp=<rows>.  None of them changes results
+// merge, nomerge, tiled, notiled, tp=<rows>, levelpass, nolevelpass.  None of them changes results
 // beyond the rounding order of the grad_value sums.
 
 struct Tune {
@@ -146,6 +146,7 @@ struct Tune {
     int merge = -1;        // backward corner merge: -1 by density, 0 off (nomerge), 1 on (merge)
     int tiled = 0;         // FP32 accumulator on chip: 0 off (notiled, the default), 1 where the shape allows (tiled)
     int lg_tp = 0;         // rows per tile of the on-chip accumulator (tp=<power of two>; 0: by D)
+    int levelpass = -1;    // backward one level at a time: -1 by size, 0 off (nolevelpass), 1 on (levelpass)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -169,6 +170,8 @@ const Tune& tune() {
             else if (!strcmp(tok, "merge")) r.merge = 1;
             else if (!strcmp(tok, "nomerge")) r.merge = 0;
             else if (!strcmp(tok, "tiled")) r.tiled = 1;
+            else if (!strcmp(tok, "levelpass")) r.levelpass = 1;
+            else if (!strcmp(tok, "nolevelpass")) r.levelpass = 0;
             else if (!strcmp(tok, "notiled")) r.tiled = 0;
             else if (!strncmp(tok, "tp=", 3)) r.lg_tp = ilog2_floor(atoi(tok + 3));
         }
@@ -362,6 +365,8 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     a.param_mode = mode;
     a.Q = (int)d.Q;
     a.det = nullptr;
+    a.s_begin = 0;
+    a.s_end = LK;
 
     pl.block = dim3(msda::kBlockThreads);
     const int64_t blocks = (d.units + tpb - 1) / tpb;
@@ -851,6 +856,38 @@ size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, i
 
 namespace {
 
+// Whether the backward runs one pass per pyramid level: the specialised
+// kernels of the unfused operator, several levels, value or the grad_value
+// accumulator larger than the L2, and enough units that each pass still
+// fills the GPU many times over (a pass gives each unit's level one team of
+// kC lanes).  Measured on GB300: encoder-scale stress backward 3.52 -> 3.15 ms
+// (FP32 accumulator) and 2.54 -> 2.19 ms (native); the odd-D workload (value
+// 267 MB, 57,600 units: under one wave per pass) 178 -> 232 us, hence the
+// unit rule.  MSDA_TUNE=levelpass / nolevelpass override both rules.
+bool level_passes(msda_dtype dt, const Dims& d, const Plan& pl, bool fused, bool use_ws, int l2_bytes, int sms) {
+    const int t = tune().levelpass;
+    if (t == 0 || !pl.spec || fused || d.L < 2) return false;
+    if (t == 1) return true;
+    const int64_t es = (int64_t)esize(dt);
+    const int64_t value_bytes = d.n_value * es, acc_bytes = d.n_value * (use_ws ? 4 : es);
+    const bool big = value_bytes > (int64_t)l2_bytes || acc_bytes > (int64_t)l2_bytes;
+    return big && d.units * msda::kC >= (int64_t)sms * 768 * 8;
+}
+
+// Launch shape of a level pass: K samples per unit, so P point lanes with
+// P * kC >= K (one lane per sample when K <= kC), and direct parameter loads
+// (a pass reads one level's parameters of each unit: a strided subset).
+void level_pass_plan(const Dims& d, Plan& pl, KernelArgs& a) {
+    const int C = 1 << a.lc;
+    int P = 1;
+    while (P * msda::kC < (int)d.K && C * P < 32) P *= 2;
+    a.lp = ilog2(P);
+    a.tpb = msda::kBlockThreads / (C * P);
+    a.param_mode = msda::PARAMS_DIRECT;
+    pl.smem = 0;
+    pl.grid = dim3((unsigned)((d.units + a.tpb - 1) / a.tpb));
+}
+
 // Backward with the FP32 accumulator on chip (msda_tiled.cuh): the gather
 // kernel without its scatter (grad_sampling_locations, grad_attention_weights),
 // then count, scan, place and accumulate for grad_value.  Nothing is enqueued
@@ -1053,7 +1090,18 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
         a.gref = fz->grad_ref;
     }
     pl.pdl = pl.spec && zeroed_here && !trace_active();
-    {
+    // One pass per pyramid level when value or the accumulator exceeds the
+    // L2: each pass's rows of the batch images in flight (value and
+    // grad_value or its workspace) then stay in the L2 between the touches of
+    // one corner row by different samples, instead of being fetched again.
+    const int passes = level_passes(dt, d, pl, fz != nullptr, use_ws, di->l2_bytes, di->sms) ? (int)d.L : 1;
+    if (passes > 1) level_pass_plan(d, pl, a);
+    for (int pass = 0; pass < passes; ++pass) {
+        if (passes > 1) {
+            a.s_begin = (int)(pass * d.K);
+            a.s_end = (int)((pass + 1) * d.K);
+            if (pass > 0) pl.pdl = false;
+        }
         TraceScope ts(st);
         switch (dt) {
         case MSDA_F32: msda::launch_backward<float, float>(a, pl, st); break;

@@ -98,6 +98,9 @@ struct KernelArgs {
     int gbuf_off;          // fused backward: byte offset of the per-sample <g, sampled> buffer in shared memory
     int rbuf_off;          // fused backward: byte offset of the per-sample grad_loc buffer, or -1 (separate kernel)
     void* gref;            // fused backward: grad_reference_points [B, Q, L, 2] (with rbuf_off >= 0)
+    // backward: the samples [s_begin, s_end) of every unit (all of them, or
+    // one level's when the backward runs one pass per level)
+    int s_begin, s_end;
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -1052,11 +1055,11 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
     if constexpr (FUSED) softmax_stats<T>(a, sm, staged, ln, smx, ssum);
     float* gbuf = reinterpret_cast<float*>(sm + a.gbuf_off) + ln.team * a.LK;  // fused: <g, sampled> per sample
 
-    for (int r0 = 0; r0 < a.LK; r0 += ln.TP) {
+    for (int r0 = a.s_begin; r0 < a.s_end; r0 += ln.TP) {
         // lane (c, p) owns sample r0 + p*kC + c: a point group's kC samples
         // are consecutive (one level's points when K = kC)
         const int s_own = r0 + ln.p * kC + ln.c;
-        const bool live = ln.active && s_own < a.LK;
+        const bool live = ln.active && s_own < a.s_end;
         float x = -4.f, y = -4.f, wa = 0.f;
         int l = 0;
         if (live) {

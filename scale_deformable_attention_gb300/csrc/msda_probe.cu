@@ -1,7 +1,8 @@
 // msda_probe.cu -- msda_reduction_ceiling: the L2's throughput for the
-// backward's kind of reduction traffic (random 32-byte sectors, each taken by
-// two adjacent 16-byte vector reductions), measured alone so that the
-// backward's scatter can be reported against it.
+// backward's kind of reduction traffic (rows of row_bytes at random places,
+// each row taken by row_bytes / 16 adjacent lanes with one 16-byte vector
+// reduction each, as a team adds one corner row of grad_value), measured
+// alone so that the backward's scatter can be reported against it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,15 +24,17 @@ __device__ __forceinline__ uint32_t scatter_hash(uint32_t x) {
     return x;
 }
 
-// Lanes 2i and 2i+1 add into the two halves of one sector, a new random
-// sector per iteration; every address is inside [buf, buf + n_sectors * 32).
+// Groups of LPR = row_bytes / 16 adjacent lanes add into one row, a new
+// random row per iteration; every address is inside [buf, buf + n_rows * row_bytes).
 template <int KIND>
-__global__ void __launch_bounds__(kProbeThreads) msda_reduction_probe_kernel(unsigned char* buf, uint32_t n_sectors) {
+__global__ void __launch_bounds__(kProbeThreads) msda_reduction_probe_kernel(unsigned char* buf, uint32_t n_rows,
+                                                                             int lg_lpr) {
     const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
-    const uint32_t pair = tid >> 1, half = tid & 1u;
+    const uint32_t grp = tid >> lg_lpr, slot = tid & ((1u << lg_lpr) - 1u);
+    const size_t row_bytes = (size_t)16 << lg_lpr;
     for (int i = 0; i < kProbeIters; ++i) {
-        const uint32_t sec = scatter_hash(pair * 1315423911u + (uint32_t)i * 2654435761u) % n_sectors;
-        unsigned char* p = buf + (size_t)sec * 32 + half * 16;
+        const uint32_t row = scatter_hash(grp * 1315423911u + (uint32_t)i * 2654435761u) % n_rows;
+        unsigned char* p = buf + (size_t)row * row_bytes + slot * 16;
         if constexpr (KIND == 0) {
             const uint32_t one = 0x3f803f80u;  // bf16x2 (1, 1)
             asm volatile("red.relaxed.gpu.global.add.noftz.v4.bf16x2 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(one), "r"(one),
@@ -50,17 +53,17 @@ __global__ void __launch_bounds__(kProbeThreads) msda_reduction_probe_kernel(uns
     }
 }
 
-void launch_probe(int kind, unsigned grid, unsigned char* buf, uint32_t n_sectors, cudaStream_t st) {
+void launch_probe(int kind, unsigned grid, unsigned char* buf, uint32_t n_rows, int lg_lpr, cudaStream_t st) {
     switch (kind) {
-    case 0: msda_reduction_probe_kernel<0><<<grid, kProbeThreads, 0, st>>>(buf, n_sectors); break;
-    case 1: msda_reduction_probe_kernel<1><<<grid, kProbeThreads, 0, st>>>(buf, n_sectors); break;
-    default: msda_reduction_probe_kernel<2><<<grid, kProbeThreads, 0, st>>>(buf, n_sectors); break;
+    case 0: msda_reduction_probe_kernel<0><<<grid, kProbeThreads, 0, st>>>(buf, n_rows, lg_lpr); break;
+    case 1: msda_reduction_probe_kernel<1><<<grid, kProbeThreads, 0, st>>>(buf, n_rows, lg_lpr); break;
+    default: msda_reduction_probe_kernel<2><<<grid, kProbeThreads, 0, st>>>(buf, n_rows, lg_lpr); break;
     }
 }
 
 }  // namespace
 
-extern "C" msda_status msda_reduction_ceiling(int kind, int blocks_per_sm, int repeats, void* scratch,
+extern "C" msda_status msda_reduction_ceiling(int kind, int row_bytes, int blocks_per_sm, int repeats, void* scratch,
                                               size_t scratch_bytes, double* sectors_per_second, msda_stream_t stream) {
     msda::clear_error();
     if (!sectors_per_second) return msda::set_error(MSDA_ERR_INVALID_ARG, "sectors_per_second is NULL");
@@ -69,8 +72,12 @@ extern "C" msda_status msda_reduction_ceiling(int kind, int blocks_per_sm, int r
     if (kind < 0 || kind > 2) return msda::set_error(MSDA_ERR_INVALID_ARG, "kind must be 0 (bf16x2), 1 (f16x2) or 2 (f32)");
     if (blocks_per_sm < 1 || blocks_per_sm > 16) return msda::set_error(MSDA_ERR_INVALID_ARG, "blocks_per_sm outside 1..16");
     if (repeats < 1 || repeats > 100) return msda::set_error(MSDA_ERR_INVALID_ARG, "repeats outside 1..100");
-    const size_t sectors64 = scratch_bytes / 32;
-    const uint32_t n_sectors = (uint32_t)(sectors64 > 0xffffffffu ? 0xffffffffu : sectors64);
+    int lg_lpr = -1;
+    for (int l = 0; l <= 5; ++l)
+        if (row_bytes == (16 << l)) lg_lpr = l;
+    if (lg_lpr < 0) return msda::set_error(MSDA_ERR_INVALID_ARG, "row_bytes must be 16, 32, 64, 128, 256 or 512");
+    const size_t rows64 = scratch_bytes / (size_t)row_bytes;
+    const uint32_t n_rows = (uint32_t)(rows64 > 0xffffffffu ? 0xffffffffu : rows64);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -84,16 +91,16 @@ extern "C" msda_status msda_reduction_ceiling(int kind, int blocks_per_sm, int r
         return msda::set_error(MSDA_ERR_CUDA, cudaGetErrorString(e));
     }
     double best = 0.0;
-    launch_probe(kind, grid, buf, n_sectors, st);  // warm-up
+    launch_probe(kind, grid, buf, n_rows, lg_lpr, st);  // warm-up
     for (int r = 0; r < repeats && e == cudaSuccess; ++r) {
         cudaEventRecord(a, st);
-        launch_probe(kind, grid, buf, n_sectors, st);
+        launch_probe(kind, grid, buf, n_rows, lg_lpr, st);
         cudaEventRecord(b, st);
         e = cudaEventSynchronize(b);
         float ms = 0.f;
         if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
         if (e == cudaSuccess && ms > 0.f) {
-            // two 16-byte reductions per sector
+            // one 16-byte reduction per lane and iteration, two per 32-byte sector
             const double sectors = (double)grid * kProbeThreads * kProbeIters / 2.0;
             const double rate = sectors / (ms * 1e-3);
             if (rate > best) best = rate;

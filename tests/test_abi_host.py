@@ -263,11 +263,13 @@ def test_binding_refuses_cpu_tensors():
 def test_reduction_ceiling_rejects_bad_arguments(lib):
     out = ctypes.c_double(0.0)
     mib = 1 << 20
-    assert lib.msda_reduction_ceiling(0, 8, 5, None, 64 * mib, ctypes.byref(out), None) == 1
+    assert lib.msda_reduction_ceiling(0, 64, 8, 5, None, 64 * mib, ctypes.byref(out), None) == 1
     assert "scratch" in msg(lib)
-    assert lib.msda_reduction_ceiling(0, 8, 5, FAKE, mib - 1, ctypes.byref(out), None) == 1
-    assert lib.msda_reduction_ceiling(0, 8, 5, FAKE + 8, 64 * mib, ctypes.byref(out), None) == 1
-    assert lib.msda_reduction_ceiling(3, 8, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1 and "kind" in msg(lib)
-    assert lib.msda_reduction_ceiling(0, 0, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1
-    assert lib.msda_reduction_ceiling(0, 8, 101, FAKE, 64 * mib, ctypes.byref(out), None) == 1
-    assert lib.msda_reduction_ceiling(0, 8, 5, FAKE, 64 * mib, None, None) == 1
+    assert lib.msda_reduction_ceiling(0, 64, 8, 5, FAKE, mib - 1, ctypes.byref(out), None) == 1
+    assert lib.msda_reduction_ceiling(0, 64, 8, 5, FAKE + 8, 64 * mib, ctypes.byref(out), None) == 1
+    assert lib.msda_reduction_ceiling(3, 64, 8, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1 and "kind" in msg(lib)
+    assert lib.msda_reduction_ceiling(0, 48, 8, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1 and "row_bytes" in msg(lib)
+    assert lib.msda_reduction_ceiling(0, 1024, 8, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1
+    assert lib.msda_reduction_ceiling(0, 64, 0, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1
+    assert lib.msda_reduction_ceiling(0, 64, 8, 101, FAKE, 64 * mib, ctypes.byref(out), None) == 1
+    assert lib.msda_reduction_ceiling(0, 64, 8, 5, FAKE, 64 * mib, None, None) == 1

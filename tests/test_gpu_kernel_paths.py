@@ -4,7 +4,8 @@ the generic one is chosen (small one-slot 16-bit problems), direct (unstaged)
 parameter loads, the staged loads without the bulk copy, the backward's
 corner merge forced on and off, ordinary (non-programmatic) launches, and
 the FP32 accumulator on chip forced on (with tiles of 16 rows: most points
-straddle tiles) and off.  Each runs in a
+straddle tiles) and off, and the backward run one pass per level (with and
+without the corner merge) or in one pass.  Each runs in a
 child process with MSDA_TUNE set."""
 import os
 import subprocess
@@ -17,7 +18,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel",
-                                  "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled"])
+                                  "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled",
+                                  "levelpass", "levelpass,merge", "nolevelpass"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
