@@ -110,6 +110,14 @@ typedef enum {
 
 /* Flags of msda_backward. */
 #define MSDA_BWD_ACCUMULATE 1u  /* add this call's gradient to grad_value instead of overwriting it */
+/* The FP32 accumulator's workspace holds zeros on entry: the call does not
+ * clear it, and its rounding pass writes zeros back over every part of it
+ * that it found non-zero, so the workspace again holds zeros on return.
+ * For a caller that allocates the workspace once, clears it once and passes
+ * it to every call (one call at a time): the separate clearing pass over the
+ * whole workspace is saved.  Ignored unless the resolved accumulator is FP32
+ * for fp16 / bf16 I/O. */
+#define MSDA_BWD_WORKSPACE_ZEROED 2u
 
 /*
  * Forward (course ch. 4, "The forward kernel, line by line"; README,
@@ -131,7 +139,8 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
                          const void* attention_weights, void* out, msda_stream_t stream);
 
 /* Workspace bytes msda_backward needs for (dt, mode) and the value size:
- * B*S*M*D*4 when the resolved accumulator is FP32 for fp16/bf16,
+ * B*S*M*D*4 when the resolved accumulator is FP32 for fp16/bf16 (less with
+ * the on-chip accumulator that MSDA_TUNE=tiled selects),
  * 256 + B*S*M*D*8 for DETERMINISTIC, else 0. */
 size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
                                     int64_t L, int64_t K, int64_t Q);
@@ -168,7 +177,9 @@ msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t
  *
  * `workspace` (device, 16-byte aligned, >= msda_backward_workspace_size()
  * bytes) is used only by the FP32 and DETERMINISTIC accumulators and may be
- * NULL otherwise; its contents on entry are irrelevant and are clobbered.
+ * NULL otherwise; its contents on entry are irrelevant and are clobbered,
+ * except with MSDA_BWD_WORKSPACE_ZEROED (FP32 accumulator: zeros on entry and
+ * on return).
  * B == 0, Q == 0, M == 0 or D == 0: nothing is sampled and every gradient
  * is zero (grad_value keeps its contents with MSDA_BWD_ACCUMULATE).
  * Requirements as msda_forward.
@@ -252,7 +263,9 @@ msda_status msda_backward_fused(msda_dtype dt, msda_accum mode, unsigned flags, 
  * made while `stream` is being captured uses the address found by the last
  * uncaptured call on that device, so make one such call first.  All calls
  * share the one array: calls that can overlap on the GPU race and must be
- * serialised by the caller.  Other arguments and errors as msda_backward.
+ * serialised by the caller.  MSDA_BWD_WORKSPACE_ZEROED is rejected
+ * (MSDA_ERR_INVALID_ARG): every call clears the array itself.  Other
+ * arguments and errors as msda_backward.
  */
 #define MSDA_STATIC_WORKSPACE_BYTES (64u << 20)
 msda_status msda_backward_static_workspace(msda_dtype dt, unsigned flags, int64_t B, int64_t S, int64_t M, int64_t D,

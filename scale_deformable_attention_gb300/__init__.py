@@ -31,7 +31,7 @@ from typing import Optional, Tuple
 import torch
 
 from . import _lib
-from ._lib import ACCUM, BWD_ACCUMULATE, MsdaError
+from ._lib import ACCUM, BWD_ACCUMULATE, BWD_WORKSPACE_ZEROED, MsdaError
 
 __all__ = ["multi_scale_deformable_attention", "multi_scale_deformable_attention_fused", "forward", "backward",
            "forward_fused", "backward_fused", "workspace_size", "resolve_accum",
@@ -201,13 +201,15 @@ def _aligned16(*ts) -> bool:
 def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_index: Optional[torch.Tensor],
              sampling_locations: torch.Tensor, attention_weights: torch.Tensor, grad_out: torch.Tensor, *,
              accum: str = "auto", grad_value: Optional[torch.Tensor] = None, accumulate: bool = False,
-             workspace: Optional[torch.Tensor] = None, validate: bool = True
+             workspace: Optional[torch.Tensor] = None, workspace_zeroed: bool = False, validate: bool = True
              ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """(grad_value, grad_sampling_locations, grad_attention_weights) (C ABI ``msda_backward``).
 
     ``accum``: "auto" | "native" | "fp32" accumulator of grad_value for fp16 / bf16, or
     "deterministic" (any dtype: run-to-run bit-identical grad_value).
     ``accumulate``: add into the given ``grad_value`` instead of overwriting it.
+    ``workspace_zeroed``: the given ``workspace`` holds zeros, and is left holding zeros
+    (MSDA_BWD_WORKSPACE_ZEROED: a persistent workspace skips the FP32 accumulator's clearing pass).
     """
     value, ss, lsi, loc, attn, dims = _prepare(value, spatial_shapes, level_start_index, sampling_locations,
                                                attention_weights, validate)
@@ -229,7 +231,9 @@ def backward(value: torch.Tensor, spatial_shapes: torch.Tensor, level_start_inde
     if need and workspace is None:
         workspace = torch.empty((need + 3) // 4, dtype=torch.float32, device=value.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    flags = BWD_ACCUMULATE if accumulate else 0
+    if workspace_zeroed and workspace is None:
+        raise ValueError("workspace_zeroed=True needs the workspace it describes")
+    flags = (BWD_ACCUMULATE if accumulate else 0) | (BWD_WORKSPACE_ZEROED if workspace_zeroed else 0)
     with torch.cuda.device(value.device):
         _lib.check(_lib.lib().msda_backward(
             DTYPE_CODE[value.dtype], ACCUM[accum], flags, *dims, _ptr(value), _ptr(ss), _ptr(lsi), _ptr(loc),

@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "MSDA_OK", 1: "MSDA_ERR_INVALID_ARG", 2: "MSDA_ERR_UNSUPPORTE
 ACCUM = {"auto": 0, "native": 1, "fp32": 2, "deterministic": 3}
 ACCUM_NAMES = {v: k for k, v in ACCUM.items()}
 BWD_ACCUMULATE = 1
+BWD_WORKSPACE_ZEROED = 2
 KERNEL_NAMES = {0: "forward", 1: "backward", 2: "zero", 3: "convert", 4: "tile_count", 5: "tile_scan",
                 6: "tile_place", 7: "tile_accum"}
 

@@ -998,7 +998,7 @@ msda_status backward_tiled(msda_dtype dt, bool accumulate, const Dims& d, const 
 // Backward after argument validation; `fz` non-NULL selects the fused
 // operator (sampling_locations / attention_weights then hold offsets /
 // logits, their gradients go to grad_sampling_locations / grad_attention_weights).
-msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const Dims& d, const void* value,
+msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const Dims& d, const void* value,
                           const int64_t* spatial_shapes, const int64_t* level_start_index,
                           const void* sampling_locations, const void* attention_weights, const void* grad_out,
                           void* grad_value, void* grad_sampling_locations, void* grad_attention_weights,
@@ -1007,6 +1007,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
     msda_status s;
     const size_t es = esize(dt);
     const bool work = d.units > 0 && D > 0;
+    const bool accumulate = (flags & MSDA_BWD_ACCUMULATE) != 0;
+    const bool ws_zeroed = (flags & MSDA_BWD_WORKSPACE_ZEROED) != 0;
     const msda_accum acc = msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q);
     if (acc == MSDA_ACCUM_DETERMINISTIC && work && d.n_value > 0)
         return backward_deterministic(dt, accumulate, d, value, spatial_shapes, level_start_index, sampling_locations,
@@ -1056,7 +1058,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
     if (!use_ws) {
         if (!accumulate && (s = launch_zero(grad_value, d.n_value * (int64_t)es, di->sms, st))) return s;
     } else if (!accumulate) {
-        if ((s = launch_zero(workspace, d.n_value * 4, di->sms, st))) return s;
+        // a workspace that holds zeros on entry (MSDA_BWD_WORKSPACE_ZEROED) needs no clearing pass
+        if (!ws_zeroed && (s = launch_zero(workspace, d.n_value * 4, di->sms, st))) return s;
     } else {
         TraceScope ts(st);
         const int grid = grid_for(d.n_value, di->sms);
@@ -1074,7 +1077,7 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
     // the zero kernel was the last thing enqueued by this call: the backward
     // may be launched as its programmatic dependent (not while tracing, whose
     // events sit between the two launches)
-    const bool zeroed_here = !accumulate && (use_ws || d.n_value > 0);
+    const bool zeroed_here = !accumulate && (use_ws ? !ws_zeroed : d.n_value > 0);
     a.value = value;
     a.shapes = spatial_shapes;
     a.starts = level_start_index;
@@ -1122,12 +1125,15 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, bool accumulate, const
         TraceScope ts(st);
         const int cvec = aligned(grad_value, 16) ? 1 : 0;
         const int grid = grid_for(d.n_value / 8 + 1, di->sms);
+        // with MSDA_BWD_WORKSPACE_ZEROED the pass leaves the workspace holding zeros
+        const int rezero = ws_zeroed ? 1 : 0;
         if (dt == MSDA_F16)
-            msda::launch_convert<__half>(static_cast<const float*>(workspace), static_cast<__half*>(grad_value),
-                                         d.n_value, cvec, grid, st);
+            msda::launch_convert<__half>(static_cast<float*>(workspace), static_cast<__half*>(grad_value), d.n_value,
+                                         cvec, rezero, grid, st);
         else
-            msda::launch_convert<__nv_bfloat16>(static_cast<const float*>(workspace),
-                                                static_cast<__nv_bfloat16*>(grad_value), d.n_value, cvec, grid, st);
+            msda::launch_convert<__nv_bfloat16>(static_cast<float*>(workspace),
+                                                static_cast<__nv_bfloat16*>(grad_value), d.n_value, cvec, rezero,
+                                                grid, st);
         ts.end(MSDA_KERNEL_CONVERT, d.n_value);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
@@ -1147,7 +1153,8 @@ msda_status backward_checks(msda_dtype dt, msda_accum mode, unsigned flags, Dims
     if (mode != MSDA_ACCUM_AUTO && mode != MSDA_ACCUM_NATIVE && mode != MSDA_ACCUM_FP32 &&
         mode != MSDA_ACCUM_DETERMINISTIC)
         return fail(MSDA_ERR_INVALID_ARG, "unknown accumulator mode %d", (int)mode);
-    if (flags & ~MSDA_BWD_ACCUMULATE) return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (flags & ~(MSDA_BWD_ACCUMULATE | MSDA_BWD_WORKSPACE_ZEROED))
+        return fail(MSDA_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     const size_t es = esize(dt);
     const bool work = d.units > 0 && d.D > 0;
     if ((s = check_ptr(grad_value, d.n_value > 0, es, "grad_value"))) return s;
@@ -1181,7 +1188,7 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
                                     grad_value, grad_sampling_locations, "grad_sampling_locations",
                                     grad_attention_weights, "grad_attention_weights");
     if (s != MSDA_OK) return s;
-    return backward_core(dt, mode, (flags & MSDA_BWD_ACCUMULATE) != 0, d, value, spatial_shapes, level_start_index,
+    return backward_core(dt, mode, flags, d, value, spatial_shapes, level_start_index,
                          sampling_locations, attention_weights, grad_out, grad_value, grad_sampling_locations,
                          grad_attention_weights, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
                          nullptr);
@@ -1209,7 +1216,7 @@ msda_status msda_backward_fused(msda_dtype dt, msda_accum mode, unsigned flags, 
         (s = check_ptr(spatial_shapes, nref, 8, "spatial_shapes")))
         return s;
     const Fused fz{reference_points, grad_reference_points};
-    return backward_core(dt, mode, (flags & MSDA_BWD_ACCUMULATE) != 0, d, value, spatial_shapes, level_start_index,
+    return backward_core(dt, mode, flags, d, value, spatial_shapes, level_start_index,
                          sampling_offsets, attention_logits, grad_out, grad_value, grad_sampling_offsets,
                          grad_attention_logits, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
                          &fz);

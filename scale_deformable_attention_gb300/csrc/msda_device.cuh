@@ -1650,24 +1650,41 @@ __global__ void __launch_bounds__(kBlockThreads) msda_det_convert_kernel(const l
 // ---------------------------------------------------------------------------
 // zero / convert helpers of the backward
 
-// grad_value[i] = round(ws[i]) for i < n (8 elements per step when aligned)
+// grad_value[i] = round(ws[i]) for i < n (8 elements per step when aligned).
+// rezero: write zeros back over every 32-byte piece of ws found non-zero, so
+// a workspace that held zeros before the backward holds zeros again (the
+// pieces no sample touched are left alone, unwritten).
 template <typename T>
-__global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(const float* ws, T* gv, long long n, int vec) {
+__global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, T* gv, long long n, int vec,
+                                                                     int rezero) {
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nth = (long long)gridDim.x * blockDim.x;
     long long done = 0;
     if (vec) {
         const long long n8 = n / 8;
-        const float4* s = reinterpret_cast<const float4*>(ws);
+        float4* s = reinterpret_cast<float4*>(ws);
         for (long long i = tid; i < n8; i += nth) {
             const float4 a = __ldcs(s + 2 * i);
             const float4 b = __ldcs(s + 2 * i + 1);
             const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             Slot<T, 8>::store(gv + 8 * i, f);
+            if (rezero) {
+                const uint32_t nz = __float_as_uint(a.x) | __float_as_uint(a.y) | __float_as_uint(a.z) |
+                                    __float_as_uint(a.w) | __float_as_uint(b.x) | __float_as_uint(b.y) |
+                                    __float_as_uint(b.z) | __float_as_uint(b.w);
+                if (nz) {
+                    __stcs(s + 2 * i, make_float4(0.f, 0.f, 0.f, 0.f));
+                    __stcs(s + 2 * i + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+                }
+            }
         }
         done = n8 * 8;
     }
-    for (long long i = done + tid; i < n; i += nth) gv[i] = Elem<T>::from_f(ws[i]);
+    for (long long i = done + tid; i < n; i += nth) {
+        const float v = ws[i];
+        gv[i] = Elem<T>::from_f(v);
+        if (rezero && __float_as_uint(v)) ws[i] = 0.f;
+    }
 }
 
 // ws[i] = grad_value[i] (accumulating backward with the fp32 workspace)

@@ -175,8 +175,8 @@ void launch_det_convert(const long long* ws, T* gv, long long n, const DetHeader
 }
 
 template <typename T>
-void launch_convert(const float* ws, T* gv, long long n, int vec, int grid, cudaStream_t st) {
-    msda_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, vec);
+void launch_convert(float* ws, T* gv, long long n, int vec, int rezero, int grid, cudaStream_t st) {
+    msda_convert_kernel<T><<<grid, kBlockThreads, 0, st>>>(ws, gv, n, vec, rezero);
 }
 
 template <typename T>
@@ -247,7 +247,7 @@ MSDA_EXTERN_IO(__nv_bfloat16)
 #undef MSDA_EXTERN_IO
 #define MSDA_EXTERN_HALF(T)                                                                              \
     extern template void launch_backward<T, T>(const KernelArgs&, const Plan&, cudaStream_t);           \
-    extern template void launch_convert<T>(const float*, T*, long long, int, int, cudaStream_t);        \
+    extern template void launch_convert<T>(float*, T*, long long, int, int, int, cudaStream_t);         \
     extern template void launch_widen<T>(const T*, float*, long long, int, cudaStream_t);
 MSDA_EXTERN_HALF(__half)
 MSDA_EXTERN_HALF(__nv_bfloat16)

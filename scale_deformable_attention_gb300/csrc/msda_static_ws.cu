@@ -75,6 +75,13 @@ extern "C" msda_status msda_backward_static_workspace(
     const void* value, const int64_t* spatial_shapes, const int64_t* level_start_index,
     const void* sampling_locations, const void* attention_weights, const void* grad_out, void* grad_value,
     void* grad_sampling_locations, void* grad_attention_weights, msda_stream_t stream) {
+    // The array is cleared by every call that uses it; a caller cannot vouch
+    // for its contents, so the flag that says the workspace holds zeros is
+    // not for this entry point.
+    if (flags & MSDA_BWD_WORKSPACE_ZEROED)
+        return msda::set_error(MSDA_ERR_INVALID_ARG,
+                               "msda_backward_static_workspace: MSDA_BWD_WORKSPACE_ZEROED does not apply to the "
+                               "library's own array");
     // First the call without scratch.  msda_backward checks every argument
     // before it enqueues anything, and asks for a workspace (MSDA_ERR_WORKSPACE)
     // only after they all pass and only when there is something to sample;

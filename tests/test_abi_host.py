@@ -137,6 +137,7 @@ def test_forward_empty_is_ok_without_launch(lib, kw):
 def test_backward_rejects_mode_and_flags(lib):
     assert bwd(lib, mode=5) == 1 and "accumulator" in msg(lib)
     assert bwd(lib, flags=4) == 1 and "flags" in msg(lib)
+    assert bwd(lib, flags=8) == 1 and "flags" in msg(lib)
 
 
 def test_backward_deterministic_needs_workspace(lib):
@@ -273,3 +274,12 @@ def test_reduction_ceiling_rejects_bad_arguments(lib):
     assert lib.msda_reduction_ceiling(0, 64, 0, 5, FAKE, 64 * mib, ctypes.byref(out), None) == 1
     assert lib.msda_reduction_ceiling(0, 64, 8, 101, FAKE, 64 * mib, ctypes.byref(out), None) == 1
     assert lib.msda_reduction_ceiling(0, 64, 8, 5, FAKE, 64 * mib, None, None) == 1
+
+def test_static_workspace_rejects_zeroed_flag(lib):
+    """The allocation-free backward clears its own array on every call; the
+    flag by which a caller vouches for a zeroed workspace does not apply."""
+    f = lib.msda_backward_static_workspace
+    f.argtypes = ([ctypes.c_int, ctypes.c_uint] + [ctypes.c_int64] * 7 + [ctypes.c_void_p] * 9 + [ctypes.c_void_p])
+    f.restype = ctypes.c_int
+    p = [FAKE] * 9
+    assert f(2, 2, 1, 4, 1, 32, 1, 1, 1, *p, None) == 1 and "ZEROED" in msg(lib)

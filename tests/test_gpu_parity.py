@@ -404,3 +404,34 @@ def test_clustered_samples_merge(dtype, accum, tune_merge):
     assert_grad(dtype, f64(gl), rgl, "clustered grad_loc")
     assert_grad(dtype, f64(ga), rga, "clustered grad_attn")
     assert msda.device_errors(clear=False) == 0
+
+
+@pytest.mark.parametrize("dtype,accumulate", [("bf16", False), ("f16", False), ("bf16", True)])
+def test_workspace_zeroed_flag(dtype, accumulate):
+    """MSDA_BWD_WORKSPACE_ZEROED: a persistent fp32 workspace, cleared once,
+    passed to three calls in a row on different inputs.  Each call matches the
+    oracle and leaves the workspace holding zeros for the next one."""
+    msda = _msda()
+    ws = None
+    for seed in (41, 42, 43):
+        wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, B=2, Q=120, seed=seed)
+        inp = W.make_inputs(wl)
+        t = to_torch(inp, dtype, DEV)
+        dims = (wl.B, wl.S, wl.M, wl.D, wl.L, wl.K, wl.Qn)
+        if ws is None:
+            ws = torch.zeros(msda.workspace_size(t["value"].dtype, "fp32", dims) // 4, dtype=torch.float32,
+                             device=DEV)
+            assert ws.numel() * 4 >= wl.B * wl.S * wl.M * wl.D * 4
+        start = torch.randn(t["value"].shape, generator=torch.Generator().manual_seed(seed)).to(DEV).to(
+            t["value"].dtype) if accumulate else None
+        gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                                   t["attention_weights"], t["grad_out"], accum="fp32",
+                                   grad_value=start.clone() if accumulate else None, accumulate=accumulate,
+                                   workspace=ws, workspace_zeroed=True)
+        torch.cuda.synchronize()
+        rgv, rgl, rga = oracle.backward(inp, dtype)
+        want = rgv + (f64(start) if accumulate else 0.0)
+        assert_grad(dtype, f64(gv), want, f"zeroed workspace seed {seed} grad_value")
+        assert_grad(dtype, f64(gl), rgl, f"zeroed workspace seed {seed} grad_loc")
+        assert_grad(dtype, f64(ga), rga, f"zeroed workspace seed {seed} grad_attn")
+        assert int(torch.count_nonzero(ws)) == 0, "the workspace must hold zeros after the call"
