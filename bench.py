@@ -158,15 +158,16 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str, accum: str):
-    """DRAM bytes per launch from a committed ncu capture, if it was taken on
-    the kernel source as it is now."""
+    """DRAM bytes per step of a kernel (its launches of one step together; per
+    launch when it launches once) from a committed ncu capture, if it was
+    taken on the kernel source as it is now."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
         e = d[f"{workload}/{accum}/{kernel}"]
         if e.get("source_hash") == kernel_source_hash():
-            return float(e["dram_bytes_per_launch"])
+            return float(e.get("dram_bytes_per_step", e.get("dram_bytes_per_launch")))
     except Exception:
         pass
     return None
@@ -476,13 +477,23 @@ def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2
     per-launch ratio when it launches once per step, and the launch-weighted
     one when it launches once per level."""
     peak, peak_kind = peaks()
-    k = kernels[dom]
+    k = dict(kernels[dom])
+    name = dom
     # the backward kernel without its scatter when the accumulate pass holds grad_value
     alg = model["backward_gather"] if dom == "backward" and "tile_accum" in per else model[dom]
+    if dom == "backward" and "convert" in kernels and accum == "fp32" and wl.dtype != "f32":
+        # FP32 accumulator: the backward passes round most of the workspace
+        # themselves (extra blocks in the passes of the coarse levels), so the
+        # rounding is counted with them: their bytes and their time together
+        name = "backward+convert"
+        alg = model["backward"] + model["convert"]
+        c = kernels["convert"]
+        k = {"avg_ms": None, "launches": k["launches"] + c["launches"], "steps": k.get("steps", 1),
+             "ms_per_step": round(k["ms_per_step"] + c["ms_per_step"], 5)}
     achieved = alg / (k["ms_per_step"] / 1e3) / 1e9
-    roof = {"kernel": dom, "bound": bound_of(dom, wl, accum, l2, "tile_accum" in per), "achieved": round(achieved, 1),
-            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic(dom, wl.name, accum),
+    roof = {"kernel": name, "bound": bound_of(dom, wl, accum, l2, "tile_accum" in per),
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(name, wl.name, accum),
             "algorithmic_bytes": alg, "bytes_model": "per-corner (every in-level corner row each time)",
             "avg_launch_ms": k["avg_ms"], "launches_per_step": round(k["launches"] / max(1, k.get("steps", 1)), 3),
             "ms_per_step": k["ms_per_step"], "peak_source": peak_kind, "launches_traced": k["launches"]}

@@ -1099,27 +1099,71 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // one corner row by different samples, instead of being fetched again.
     const int passes = level_passes(dt, d, pl, fz != nullptr, use_ws, di->l2_bytes, di->sms) ? (int)d.L : 1;
     if (passes > 1) level_pass_plan(d, pl, a);
+    // With one pass per level, the FP32 workspace's rows below the first row
+    // of level 2 are final once passes 0 and 1 are done: the passes from
+    // level 2 on (L2-bound, DRAM mostly idle) round them with extra blocks,
+    // and the rounding pass afterwards handles the remaining rows only.
+    constexpr int kFoldLevel = 2;
+    constexpr long long kFoldChunk = 1 << 16;   // workspace elements per folding block
+    const bool fold = passes > 1 && use_ws && d.L > kFoldLevel && pl.spec && fz == nullptr &&
+                      aligned(grad_value, 16) && (d.S * d.M * d.D) % 8 == 0;
+    long long fold_chunks = 0;
+    if (fold) {
+        a.conv_level = kFoldLevel;
+        a.conv_rezero = ws_zeroed ? 1 : 0;
+        a.conv_out = grad_value;
+        a.n_images = (int)d.B;
+        a.conv_chunk = kFoldChunk;
+        a.conv_chunks_per_image = (a.slice + kFoldChunk - 1) / kFoldChunk;
+        fold_chunks = d.B * a.conv_chunks_per_image;
+    }
     for (int pass = 0; pass < passes; ++pass) {
+        Plan lp = pl;
+        a.conv_blocks = 0;
         if (passes > 1) {
             a.s_begin = (int)(pass * d.K);
             a.s_end = (int)((pass + 1) * d.K);
-            if (pass > 0) pl.pdl = false;
+            if (pass > 0) lp.pdl = false;
+            if (fold && pass >= kFoldLevel) {
+                // this pass's share of the chunks, interleaved with its sampling blocks
+                const int hosts = passes - kFoldLevel, h = pass - kFoldLevel;
+                const long long c0 = fold_chunks * h / hosts, c1 = fold_chunks * (h + 1) / hosts;
+                const long long ns = pl.grid.x, nc = c1 - c0;
+                if (nc > 0 && ns + nc < 0x7fffffffLL) {
+                    a.conv_blocks = (int)nc;
+                    a.conv_first = c0;
+                    a.conv_every = (int)((ns + nc) / nc);
+                    lp.grid = dim3((unsigned)(ns + nc));
+                }
+            }
         }
         TraceScope ts(st);
         switch (dt) {
-        case MSDA_F32: msda::launch_backward<float, float>(a, pl, st); break;
+        case MSDA_F32: msda::launch_backward<float, float>(a, lp, st); break;
         case MSDA_F16:
-            if (use_ws) msda::launch_backward<__half, float>(a, pl, st);
-            else msda::launch_backward<__half, __half>(a, pl, st);
+            if (use_ws) msda::launch_backward<__half, float>(a, lp, st);
+            else msda::launch_backward<__half, __half>(a, lp, st);
             break;
         default:
-            if (use_ws) msda::launch_backward<__nv_bfloat16, float>(a, pl, st);
-            else msda::launch_backward<__nv_bfloat16, __nv_bfloat16>(a, pl, st);
+            if (use_ws) msda::launch_backward<__nv_bfloat16, float>(a, lp, st);
+            else msda::launch_backward<__nv_bfloat16, __nv_bfloat16>(a, lp, st);
             break;
         }
         ts.end(MSDA_KERNEL_BACKWARD, d.units);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
+    }
+    if (use_ws && fold) {
+        // the rows from the first row of level 2 on, in every batch image
+        TraceScope ts(st);
+        const int grid = grid_for(d.n_value / 8 / 16 + 1, di->sms);
+        if (dt == MSDA_F16) msda::launch_convert_tail<__half>(a, grid, st);
+        else msda::launch_convert_tail<__nv_bfloat16>(a, grid, st);
+        ts.end(MSDA_KERNEL_CONVERT, d.n_value);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
+        if (fz && a.rbuf_off < 0) return launch_ref_grad(dt, d, spatial_shapes, grad_sampling_locations, fz->grad_ref, st);
+        return MSDA_OK;
     }
     if (use_ws) {
         TraceScope ts(st);

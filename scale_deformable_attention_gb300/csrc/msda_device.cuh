@@ -101,6 +101,16 @@ struct KernelArgs {
     // backward: the samples [s_begin, s_end) of every unit (all of them, or
     // one level's when the backward runs one pass per level)
     int s_begin, s_end;
+    // Rounding of the fp32 workspace folded into a backward pass (FP32
+    // accumulator, one pass per level): conv_blocks blocks of the launch,
+    // every conv_every-th one, each round one chunk of conv_chunk workspace
+    // elements into grad_value (conv_out), restricted to the pyramid rows
+    // below the first row of levels >= conv_level, which no pass from
+    // conv_level on adds to.  conv_first: this launch's first chunk.
+    int conv_blocks, conv_every, conv_level, conv_rezero;
+    long long conv_first, conv_chunk, conv_chunks_per_image;
+    void* conv_out;
+    int n_images;          // B
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -479,7 +489,7 @@ struct Lane {
     uint32_t u0, u;
     bool active;
 };
-__device__ __forceinline__ Lane lane_of(const KernelArgs& a) {
+__device__ __forceinline__ Lane lane_of(const KernelArgs& a, uint32_t blk) {
     Lane r;
     const int lcp = a.lc + a.lp;
     r.C = 1 << a.lc;
@@ -489,11 +499,12 @@ __device__ __forceinline__ Lane lane_of(const KernelArgs& a) {
     const int lt = threadIdx.x & (r.TP - 1);
     r.c = lt & (r.C - 1);
     r.p = lt >> a.lc;
-    r.u0 = blockIdx.x * (uint32_t)a.tpb;
+    r.u0 = blk * (uint32_t)a.tpb;
     r.u = r.u0 + r.team;
     r.active = r.u < (uint32_t)a.n_units;
     return r;
 }
+__device__ __forceinline__ Lane lane_of(const KernelArgs& a) { return lane_of(a, blockIdx.x); }
 
 // ---------------------------------------------------------------------------
 // forward (course ch. 4; README "Kernel design" item 1)
@@ -967,6 +978,52 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
     }
 }
 
+// Eight workspace elements from index 8*i: rounded once into grad_value; with
+// rezero, the 32 bytes written back as zeros when any of them is non-zero.
+template <typename T>
+__device__ __forceinline__ void round8(float* ws, T* gv, long long i, int rezero) {
+    float4* s = reinterpret_cast<float4*>(ws);
+    const float4 x = __ldcs(s + 2 * i);
+    const float4 y = __ldcs(s + 2 * i + 1);
+    const float f[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+    Slot<T, 8>::store(gv + 8 * i, f);
+    if (rezero) {
+        const uint32_t nz = __float_as_uint(x.x) | __float_as_uint(x.y) | __float_as_uint(x.z) | __float_as_uint(x.w) |
+                            __float_as_uint(y.x) | __float_as_uint(y.y) | __float_as_uint(y.z) | __float_as_uint(y.w);
+        if (nz) {
+            __stcs(s + 2 * i, make_float4(0.f, 0.f, 0.f, 0.f));
+            __stcs(s + 2 * i + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+    }
+}
+
+// The first pyramid row of the levels >= l0 that pass the shape check (S if
+// none): rows below it receive nothing from those levels.
+__device__ __forceinline__ long long first_row_from(const KernelArgs& a, int l0) {
+    long long p = a.S;
+    for (int l = l0; l < a.L; ++l) {
+        const long long H = a.shapes[2 * l], W = a.shapes[2 * l + 1], st = a.starts[l];
+        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
+                        H * W <= a.S - st;
+        if (ok && st < p) p = st;
+    }
+    return p;
+}
+
+// One folded chunk: workspace elements [k*conv_chunk, (k+1)*conv_chunk) of
+// batch image img, cut at the first row of the levels >= conv_level.
+template <typename T>
+__device__ __noinline__ void fold_round_chunk(const KernelArgs& a, long long c) {
+    __shared__ long long cut;
+    if (threadIdx.x == 0) cut = first_row_from(a, a.conv_level) * a.M * a.D;
+    __syncthreads();
+    const long long img = c / a.conv_chunks_per_image, k = c - img * a.conv_chunks_per_image;
+    const long long e0 = k * a.conv_chunk, e1 = min(e0 + a.conv_chunk, cut);
+    float* ws = reinterpret_cast<float*>(a.grad_acc) + img * a.slice;
+    T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
+    for (long long i = e0 / 8 + threadIdx.x; i < e1 / 8; i += blockDim.x) round8<T>(ws, gv, i, a.conv_rezero);
+}
+
 // Backward, same decomposition.  Each round first gathers the corners of its
 // samples and reduces <g, corner> to grad_attn / grad_loc (reads only), then
 // scatters grad_value.  When launched as a programmatic dependent of the
@@ -990,7 +1047,21 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
     __shared__ int verdict;
     extern __shared__ __align__(16) unsigned char sm[];
 
-    const Lane ln = lane_of(a);
+    // Blocks that round finished workspace rows instead of sampling (the
+    // rounding pass folded into this launch; see KernelArgs::conv_blocks):
+    // every conv_every-th block, so they run alongside the sampling blocks.
+    uint32_t blk = blockIdx.x;
+    if constexpr (std::is_same<ACC, float>::value && sizeof(T) == 2 && !FUSED) {
+        if (a.conv_blocks > 0) {
+            const uint32_t R = (uint32_t)a.conv_every;
+            if (blk % R == R - 1 && blk / R < (uint32_t)a.conv_blocks) {
+                fold_round_chunk<T>(a, a.conv_first + blk / R);
+                return;
+            }
+            blk -= min((blk + 1) / R, (uint32_t)a.conv_blocks);
+        }
+    }
+    const Lane ln = lane_of(a, blk);
     if (!prologue<T>(a, lv, sm, &bar, &verdict, ln.u0)) {
         if (threadIdx.x == 0) atomicOr(a.err, kErrBulkTimeout);
         return;
@@ -1662,28 +1733,31 @@ __global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, 
     long long done = 0;
     if (vec) {
         const long long n8 = n / 8;
-        float4* s = reinterpret_cast<float4*>(ws);
-        for (long long i = tid; i < n8; i += nth) {
-            const float4 a = __ldcs(s + 2 * i);
-            const float4 b = __ldcs(s + 2 * i + 1);
-            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            Slot<T, 8>::store(gv + 8 * i, f);
-            if (rezero) {
-                const uint32_t nz = __float_as_uint(a.x) | __float_as_uint(a.y) | __float_as_uint(a.z) |
-                                    __float_as_uint(a.w) | __float_as_uint(b.x) | __float_as_uint(b.y) |
-                                    __float_as_uint(b.z) | __float_as_uint(b.w);
-                if (nz) {
-                    __stcs(s + 2 * i, make_float4(0.f, 0.f, 0.f, 0.f));
-                    __stcs(s + 2 * i + 1, make_float4(0.f, 0.f, 0.f, 0.f));
-                }
-            }
-        }
+        for (long long i = tid; i < n8; i += nth) round8<T>(ws, gv, i, rezero);
         done = n8 * 8;
     }
     for (long long i = done + tid; i < n; i += nth) {
         const float v = ws[i];
         gv[i] = Elem<T>::from_f(v);
         if (rezero && __float_as_uint(v)) ws[i] = 0.f;
+    }
+}
+
+// The rounding pass for the rows the backward passes did not round
+// themselves: in every batch image, the rows from the first row of the levels
+// >= a.conv_level on (16-byte aligned workspace and grad_value, slices of a
+// multiple of 8 elements).
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_convert_tail_kernel(const KernelArgs a) {
+    __shared__ long long cut;
+    if (threadIdx.x == 0) cut = first_row_from(a, a.conv_level) * a.M * a.D;
+    __syncthreads();
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long nth = (long long)gridDim.x * blockDim.x;
+    for (int img = 0; img < a.n_images; ++img) {
+        float* ws = reinterpret_cast<float*>(a.grad_acc) + img * a.slice;
+        T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
+        for (long long i = cut / 8 + tid; i < a.slice / 8; i += nth) round8<T>(ws, gv, i, a.conv_rezero);
     }
 }
 

@@ -180,6 +180,11 @@ void launch_convert(float* ws, T* gv, long long n, int vec, int rezero, int grid
 }
 
 template <typename T>
+void launch_convert_tail(const KernelArgs& a, int grid, cudaStream_t st) {
+    msda_convert_tail_kernel<T><<<grid, kBlockThreads, 0, st>>>(a);
+}
+
+template <typename T>
 void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st) {
     msda_widen_kernel<T><<<grid, kBlockThreads, 0, st>>>(gv, ws, n);
 }
@@ -248,7 +253,8 @@ MSDA_EXTERN_IO(__nv_bfloat16)
 #define MSDA_EXTERN_HALF(T)                                                                              \
     extern template void launch_backward<T, T>(const KernelArgs&, const Plan&, cudaStream_t);           \
     extern template void launch_convert<T>(float*, T*, long long, int, int, int, cudaStream_t);         \
-    extern template void launch_widen<T>(const T*, float*, long long, int, cudaStream_t);
+    extern template void launch_widen<T>(const T*, float*, long long, int, cudaStream_t);                \
+    extern template void launch_convert_tail<T>(const KernelArgs&, int, cudaStream_t);
 MSDA_EXTERN_HALF(__half)
 MSDA_EXTERN_HALF(__nv_bfloat16)
 #undef MSDA_EXTERN_HALF
