@@ -435,3 +435,35 @@ def test_workspace_zeroed_flag(dtype, accumulate):
         assert_grad(dtype, f64(gl), rgl, f"zeroed workspace seed {seed} grad_loc")
         assert_grad(dtype, f64(ga), rga, f"zeroed workspace seed {seed} grad_attn")
         assert int(torch.count_nonzero(ws)) == 0, "the workspace must hold zeros after the call"
+
+
+@pytest.mark.parametrize("levels_reversed,zeroed", [(False, False), (True, False), (False, True)])
+def test_level_passes_round_finished_rows(levels_reversed, zeroed):
+    """A problem large enough for one backward pass per level (the fp32
+    workspace exceeds the L2, and there are many units): the passes of the
+    coarse levels round the workspace rows below the first row of level 2.
+    With the levels stored in reverse order in the pyramid that cut is row 0,
+    so every row is left to the rounding pass.  Both against the oracle, with
+    and without a workspace that holds zeros on entry (and must on return)."""
+    msda = _msda()
+    shapes = ((256, 256), (128, 128), (64, 64), (32, 32))
+    wl = W.WORKLOADS["decoder_bf16"].with_(B=2, Q=15000, shapes=shapes, seed=51)
+    assert wl.B * wl.S * wl.M * wl.D * 4 > 160e6 and wl.units * 4 > 8 * 152 * 768
+    inp = dict(W.make_inputs(wl))
+    if levels_reversed:
+        hw = [h * w for h, w in shapes]
+        inp["level_start_index"] = np.array([sum(hw[l + 1:]) for l in range(4)], dtype=np.int64)
+    t = to_torch(inp, "bf16", DEV)
+    dims = (wl.B, wl.S, wl.M, wl.D, wl.L, wl.K, wl.Qn)
+    ws = torch.zeros(msda.workspace_size(torch.bfloat16, "fp32", dims) // 4, dtype=torch.float32, device=DEV)
+    for _ in range(2):
+        gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                                   t["attention_weights"], t["grad_out"], accum="fp32", workspace=ws,
+                                   workspace_zeroed=zeroed)
+        torch.cuda.synchronize()
+        if zeroed:
+            assert int(torch.count_nonzero(ws)) == 0
+    rgv, rgl, rga = oracle.backward(inp, "bf16")
+    assert_grad("bf16", f64(gv), rgv, "grad_value")
+    assert_grad("bf16", f64(gl), rgl, "grad_loc")
+    assert_grad("bf16", f64(ga), rga, "grad_attn")
