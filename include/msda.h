@@ -206,8 +206,8 @@ msda_status msda_backward(msda_dtype dt, msda_accum mode, unsigned flags, int64_
  *
  * Layouts: reference_points [B, Q, L, 2] (x, y); sampling_offsets
  * [B, Q, M, L, K, 2]; attention_logits [B, Q, M, L*K]; out [B, Q, M*D].
- * Needs rows of whole 16-byte vectors (D*esize in {64, 128, 192} bytes:
- * D = 32/64/96 for bf16/fp16, 16/32/48 for fp32) and 16-byte aligned value /
+ * Needs rows of whole 16-byte vectors (D*esize in {64, 128, 192, 256} bytes:
+ * D = 32/64/96/128 for bf16/fp16, 16/32/48/64 for fp32) and 16-byte aligned value /
  * out / grad pointers; otherwise MSDA_ERR_UNSUPPORTED.  Other requirements
  * and errors as msda_forward.
  */

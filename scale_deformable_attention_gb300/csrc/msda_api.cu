@@ -304,7 +304,8 @@ void pick_c(int nvec, int* C, int* NV) {
 }
 
 msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool backward, const void* loc,
-                      const void* attn, Plan& pl, KernelArgs& a, bool fused = false, int lane_scale = 1) {
+                      const void* attn, Plan& pl, KernelArgs& a, bool fused = false, int lane_scale = 1,
+                      bool nv4 = false) {
     const int es = (int)esize(dt);
     const int epv = vec ? 16 / es : 1;
     const int nvec = (int)(d.D / epv);
@@ -377,7 +378,12 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     pl.wide = a.slice > (1ll << 30);
     pl.nv = NV;
     pl.vec = vec;
-    pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && NV <= 3 && !t.generic;
+    // four vectors a lane (256-byte rows) take the specialised kernels where
+    // they were measured faster than the generic ones: the fp32 forward and
+    // a backward into the fp32 workspace (the native 16-bit reductions are
+    // faster in the generic kernel); the fused operator has no generic kernel
+    pl.spec = vec && !pl.wide && C == msda::kC && nvec == C * NV && !t.generic &&
+              (NV <= 3 || (NV == 4 && (fused || nv4)));
     pl.pdl = false;
     pl.fused = fused;
     a.ref = nullptr;
@@ -409,7 +415,7 @@ msda_status make_plan(msda_dtype dt, const Dims& d, bool vec, int sms, bool back
     if (fused && !pl.spec)
         return fail(MSDA_ERR_UNSUPPORTED,
                     "the fused operator needs rows of whole 16-byte vectors with 16-byte aligned value / grad "
-                    "pointers and D*esize in {64, 128, 192} bytes (D = %lld)",
+                    "pointers and D*esize in {64, 128, 192, 256} bytes (D = %lld)",
                     (long long)d.D);
     return MSDA_OK;
 }
@@ -708,7 +714,8 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
     const bool big = d.n_value * (int64_t)es > (int64_t)di->l2_bytes;
     KernelArgs a{};
     Plan pl{};
-    if ((s = make_plan(dt, d, vec, di->sms, false, loc, attn, pl, a, ref != nullptr, big ? 2 : 1))) return s;
+    if ((s = make_plan(dt, d, vec, di->sms, false, loc, attn, pl, a, ref != nullptr, big ? 2 : 1, dt == MSDA_F32)))
+        return s;
     // One 16-bit slot per lane and few samples (at most 2^20): the generic
     // forward, whose lanes each set up their own samples, is faster than the
     // specialised one, whose setup-then-shuffle chain lengthens a latency-bound
@@ -907,7 +914,9 @@ msda_status backward_tiled(msda_dtype dt, bool accumulate, const Dims& d, const 
     KernelArgs a{};
     Plan pl{};
     if ((s = make_plan(dt, d, true, di->sms, true, loc, attn, pl, a, false))) return s;
-    if (!pl.spec) return fail(MSDA_ERR_UNSUPPORTED, "on-chip FP32 accumulation needs the specialised kernels");
+    // (its gather and accumulate kernels exist for one to three vectors a lane)
+    if (!pl.spec || pl.nv > 3)
+        return fail(MSDA_ERR_UNSUPPORTED, "on-chip FP32 accumulation needs the specialised kernels");
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     msda::TileArgs t{};
     t.loc = loc;
@@ -1051,7 +1060,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     KernelArgs a{};
     Plan pl{};
     // the plan first: a call it rejects enqueues nothing
-    if ((s = make_plan(dt, d, vec, di->sms, true, sampling_locations, attention_weights, pl, a, fz != nullptr)))
+    if ((s = make_plan(dt, d, vec, di->sms, true, sampling_locations, attention_weights, pl, a, fz != nullptr, 1,
+                       use_ws)))
         return s;
 
     // grad_value (or the workspace) must start from zero / from grad_value

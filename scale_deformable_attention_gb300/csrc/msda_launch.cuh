@@ -18,7 +18,7 @@ struct Plan {
     int nv;        // vectors per lane, 1..4
     bool vec;      // 16-byte slots (else one element per slot)
     bool wide;     // 64-bit offsets inside a batch slice
-    bool spec;     // specialised kernels: C = 4, nvec == 4 * nv, nv <= 3, 32-bit offsets
+    bool spec;     // specialised kernels: C = 4, nvec == 4 * nv, nv <= 4, 32-bit offsets
     bool pdl;      // launched as a programmatic dependent of the kernel ahead of it
     bool fused;    // fused operator (offsets + logits in, offset / logit gradients out)
     bool merge;    // backward: merge the corners a point group's samples share before the scatter
@@ -108,7 +108,7 @@ template <typename T>
 void launch_forward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     constexpr int VE = 16 / sizeof(T);
     if (pl.spec) {
-        MSDA_DISPATCH_NV3(pl.nv, (fwd4_go<T, NV>(a, pl, st)))
+        MSDA_DISPATCH_NV(pl.nv, (fwd4_go<T, NV>(a, pl, st)))
         return;
     }
     if (pl.vec) {
@@ -124,7 +124,7 @@ template <typename T, typename ACC>
 void launch_backward(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     constexpr int VE = 16 / sizeof(T);
     if (pl.spec) {
-        MSDA_DISPATCH_NV3(pl.nv, (bwd4_go<T, ACC, NV>(a, pl, st)))
+        MSDA_DISPATCH_NV(pl.nv, (bwd4_go<T, ACC, NV>(a, pl, st)))
         return;
     }
     if (pl.vec) {

@@ -23,6 +23,7 @@ def main():
         ("bf16", 96, 1, "native"), ("f32", 32, 8, "auto"), ("bf16", 32, 4, "deterministic"),
         ("f32", 48, 2, "deterministic"), ("f16", 64, 4, "fp32"), ("bf16", 96, 2, "fp32"),
         ("bf16", 32, 4, "fp32"), ("f16", 32, 4, "native"), ("f32", 16, 4, "auto"),
+        ("bf16", 128, 4, "native"), ("f16", 128, 2, "fp32"), ("f32", 64, 4, "auto"),
     ]
     for dtype, D, K, accum in cases:
         wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, D=D, K=K, B=2, Q=41, M=3,

@@ -84,6 +84,10 @@ CASES = [
     ("decoder_bf16", (("dtype", "f32"), ("B", 2)), "auto"),
     ("decoder_bf16", (("dtype", "f16"), ("B", 2), ("D", 64)), "native"),
     ("decoder_bf16", (("D", 96), ("B", 2)), "fp32"),
+    ("decoder_bf16", (("D", 128), ("B", 2)), "native"),                 # 256-byte rows
+    ("decoder_bf16", (("D", 64), ("B", 2), ("dtype", "f32")), "auto"),
+    ("decoder_bf16", (("D", 128), ("B", 2), ("dtype", "f16")), "fp32"),
+    ("decoder_bf16", (("D", 128), ("B", 2)), "deterministic"),
     ("encoder_fp16", (("B", 1),), "native"),
     ("encoder_fp16", (("B", 1),), "deterministic"),
     ("oddD_fp32", (("B", 2),), "auto"),
@@ -160,7 +164,7 @@ def test_fused_empty(over):
     assert gv.abs().sum().item() == 0 and gr.numel() == 0 and go.numel() == 0 and gz.numel() == 0
 
 
-@pytest.mark.parametrize("dtype,D", [("f32", 8), ("bf16", 16), ("f32", 64), ("bf16", 5)])
+@pytest.mark.parametrize("dtype,D", [("f32", 8), ("bf16", 16), ("f32", 80), ("bf16", 5), ("bf16", 160)])
 def test_fused_rejects_rows_it_cannot_vectorise(dtype, D):
     msda = _msda()
     wl = W.WORKLOADS["tiny_fp32"].with_(dtype=dtype, D=D)
