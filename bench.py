@@ -125,7 +125,10 @@ def byte_model(wl: W.Workload, corners: int, unique_rows=None) -> dict:
            "backward_gather": gather + rowio + 2 * (loc + attn),
            "tile_accum": gather + n_value * es,
            "tile_count": loc, "tile_place": loc + 4 * wl.samples,
-           "tile_scan": 12 * wl.B * wl.M * ((wl.S + 511) // 512)}
+           "tile_scan": 12 * wl.B * wl.M * ((wl.S + 511) // 512),
+           # the touch count of the FP32 workspace's rows: the locations, and
+           # 2 bits of class per (b, pixel, head) row
+           "touch_count": loc + wl.B * wl.S * wl.M // 4}
     if unique_rows is not None:
         urow = unique_rows * wl.D * es
         out["unique_rows"] = unique_rows
@@ -439,7 +442,7 @@ def bound_of(kernel: str, wl: W.Workload, accum: str, l2: int, tiled: bool = Fal
         return "hbm" if acc_bytes > l2 else "l2"
     if kernel == "tile_accum":
         return "hbm" if value_bytes > l2 else "l2"
-    if kernel.startswith("tile_"):
+    if kernel.startswith("tile_") or kernel == "touch_count":
         return "hbm" if wl.samples * 3 * es > l2 else "l2"
     if value_bytes > l2 or (kernel == "backward" and acc_bytes > l2):
         return "hbm"

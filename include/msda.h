@@ -139,9 +139,11 @@ msda_status msda_forward(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t
                          const void* attention_weights, void* out, msda_stream_t stream);
 
 /* Workspace bytes msda_backward needs for (dt, mode) and the value size:
- * B*S*M*D*4 when the resolved accumulator is FP32 for fp16/bf16 (less with
- * the on-chip accumulator that MSDA_TUNE=tiled selects),
- * 256 + B*S*M*D*8 for DETERMINISTIC, else 0. */
+ * when the resolved accumulator is FP32 for fp16/bf16, the fp32 sums
+ * (B*S*M*D*4, rounded up to 16) followed by the touch classes of their rows
+ * (2 bits per (b, pixel, head) row: (B*S*M + 63)/64*16 bytes); less with the
+ * on-chip accumulator that MSDA_TUNE=tiled selects.  256 + B*S*M*D*8 for
+ * DETERMINISTIC, else 0. */
 size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, int64_t S, int64_t M, int64_t D,
                                     int64_t L, int64_t K, int64_t Q);
 
@@ -179,7 +181,12 @@ msda_accum msda_resolve_accum(msda_dtype dt, msda_accum mode, int64_t B, int64_t
  * bytes) is used only by the FP32 and DETERMINISTIC accumulators and may be
  * NULL otherwise; its contents on entry are irrelevant and are clobbered,
  * except with MSDA_BWD_WORKSPACE_ZEROED (FP32 accumulator: zeros on entry and
- * on return).
+ * on return).  The FP32 accumulator also runs with a workspace of the fp32
+ * sums alone (B*S*M*D*4 bytes); with the touch classes' bytes after them, a
+ * backward run one pass per level (large problems) first counts the corner
+ * contributions to the rows of the levels that take few of them, writes a row
+ * taking exactly one straight to grad_value (the one-term sum, rounded once)
+ * and reads back from the sums only the rows taking several.
  * B == 0, Q == 0, M == 0 or D == 0: nothing is sampled and every gradient
  * is zero (grad_value keeps its contents with MSDA_BWD_ACCUMULATE).
  * Requirements as msda_forward.
@@ -247,9 +254,11 @@ msda_status msda_backward_fused(msda_dtype dt, msda_accum mode, unsigned flags, 
  * allocation after start-up).  Results equal msda_backward(dt,
  * MSDA_ACCUM_FP32, flags, ...) up to the summation order of grad_value.
  *
- * Limit: the scratch that msda_backward_workspace_size(dt, MSDA_ACCUM_FP32,
- * ...) reports must fit in MSDA_STATIC_WORKSPACE_BYTES, else
- * MSDA_ERR_WORKSPACE before anything is enqueued.  The limit applies only to
+ * Limit: the FP32 accumulator's sums, B*S*M*D*4 bytes (what
+ * msda_backward_workspace_size(dt, MSDA_ACCUM_FP32, ...) reports without the
+ * touch classes, which are used when they fit as well), must fit in
+ * MSDA_STATIC_WORKSPACE_BYTES, else MSDA_ERR_WORKSPACE before anything is
+ * enqueued.  The limit applies only to
  * calls that need scratch: fp32 I/O, and calls with nothing to sample
  * (B*Q*M*D == 0), need none and have no limit.  Arguments are checked as
  * msda_backward checks them, and give its errors.
@@ -332,7 +341,7 @@ typedef struct {
 
 enum { MSDA_KERNEL_FORWARD = 0, MSDA_KERNEL_BACKWARD = 1, MSDA_KERNEL_ZERO = 2, MSDA_KERNEL_CONVERT = 3,
        MSDA_KERNEL_TILE_COUNT = 4, MSDA_KERNEL_TILE_SCAN = 5, MSDA_KERNEL_TILE_PLACE = 6,
-       MSDA_KERNEL_TILE_ACCUM = 7, MSDA_KERNEL_COUNT = 8 };
+       MSDA_KERNEL_TILE_ACCUM = 7, MSDA_KERNEL_TOUCH = 8, MSDA_KERNEL_COUNT = 9 };
 
 msda_status msda_trace_enable(int capacity);
 /* Pause (paused != 0) or resume recording without destroying the events:

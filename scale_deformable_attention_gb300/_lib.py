@@ -21,7 +21,7 @@ ACCUM_NAMES = {v: k for k, v in ACCUM.items()}
 BWD_ACCUMULATE = 1
 BWD_WORKSPACE_ZEROED = 2
 KERNEL_NAMES = {0: "forward", 1: "backward", 2: "zero", 3: "convert", 4: "tile_count", 5: "tile_scan",
-                6: "tile_place", 7: "tile_accum"}
+                6: "tile_place", 7: "tile_accum", 8: "touch_count"}
 
 
 class MsdaError(RuntimeError):

@@ -132,8 +132,8 @@ int ilog2_floor(int v) {
 // ---- tuning overrides (sweeps and tests), read once per process ----
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
 // params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
-// merge, nomerge, tiled, notiled, tp=<rows>, levelpass, nolevelpass.  None of them changes results
-// beyond the rounding order of the grad_value sums.
+// merge, nomerge, tiled, notiled, tp=<rows>, levelpass, nolevelpass, touch, notouch, tau=<n>, fold, nofold.
+// None of them changes results beyond the rounding order of the grad_value sums.
 
 struct Tune {
     int C = 0, P = 0, params = -1;
@@ -147,6 +147,9 @@ struct Tune {
     int tiled = 0;         // FP32 accumulator on chip: 0 off (notiled, the default), 1 where the shape allows (tiled)
     int lg_tp = 0;         // rows per tile of the on-chip accumulator (tp=<power of two>; 0: by D)
     int levelpass = -1;    // backward one level at a time: -1 by size, 0 off (nolevelpass), 1 on (levelpass)
+    int touch = 1;         // touch classes of the FP32 workspace's rows: 1 where they apply (touch), 0 off (notouch)
+    int tau = 0;           // sparse-level bound of the touch classes (tau=<n>; 0: the default)
+    int fold = -1;         // rounding folded into the level passes: -1 unless the touch classes apply, 0 off (nofold), 1 on (fold)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -174,6 +177,11 @@ const Tune& tune() {
             else if (!strcmp(tok, "nolevelpass")) r.levelpass = 0;
             else if (!strcmp(tok, "notiled")) r.tiled = 0;
             else if (!strncmp(tok, "tp=", 3)) r.lg_tp = ilog2_floor(atoi(tok + 3));
+            else if (!strcmp(tok, "touch")) r.touch = 1;
+            else if (!strcmp(tok, "notouch")) r.touch = 0;
+            else if (!strncmp(tok, "tau=", 4)) r.tau = atoi(tok + 4);
+            else if (!strcmp(tok, "nofold")) r.fold = 0;
+            else if (!strcmp(tok, "fold")) r.fold = 1;
         }
         return r;
     }();
@@ -255,6 +263,14 @@ struct TileLayout {
 // additions per second than the L2 does with its 16-byte vector reductions,
 // and the count and place passes wait on the counters of the coarse levels'
 // few tiles.  Its workspace is ~26x smaller (329 MB against 8.56 GB there).
+// Touch classes of the FP32 workspace's rows (msda_device.cuh, touch_sparse):
+// 2 bits per (b, pixel, head) row, placed after the B*S*M*D fp32 sums at a
+// 16-byte boundary.  A level is sparse at most kTouchTau corner contributions
+// a row on average (tau=<n> overrides).
+constexpr int kTouchTau = 4;
+size_t touch_map_offset(int64_t n_value) { return ((size_t)n_value * 4 + 15) & ~(size_t)15; }
+size_t touch_map_bytes(int64_t B, int64_t S, int64_t M) { return (size_t)((B * S * M + 63) / 64) * 16; }
+
 bool tiled_layout(msda_dtype dt, msda_accum acc, const Dims& d, bool fused, TileLayout* tl) {
     const Tune& t = tune();
     if (t.tiled != 1 || fused || acc != MSDA_ACCUM_FP32 || (dt != MSDA_F16 && dt != MSDA_BF16)) return false;
@@ -554,6 +570,18 @@ msda_status launch_zero(void* p, int64_t nbytes, int sms, cudaStream_t st) {
 namespace msda {
 msda_status set_error(msda_status s, const char* message) { return fail(s, "%s", message); }
 void clear_error() { g_msg[0] = 0; }
+
+size_t fp32_workspace_bytes(msda_dtype dt, int64_t B, int64_t S, int64_t M, int64_t D, int64_t L, int64_t K,
+                            int64_t Q, bool touch) {
+    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
+    TileLayout tl;
+    if (L >= 0 && K >= 0 && check_dims(dt, d) == MSDA_OK && tiled_layout(dt, MSDA_ACCUM_FP32, d, false, &tl))
+        return tl.bytes;
+    int64_t n;
+    if (!mul_ok(B, S, &n) || !mul_ok(n, M, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 4, &n)) return SIZE_MAX;
+    // the fp32 sums, then the touch classes of their rows
+    return touch ? touch_map_offset(n / 4) + touch_map_bytes(B, S, M) : (size_t)n;
+}
 }  // namespace msda
 
 namespace {
@@ -692,6 +720,7 @@ const char* msda_kernel_name(int k) {
     case MSDA_KERNEL_TILE_SCAN: return "tile_scan";
     case MSDA_KERNEL_TILE_PLACE: return "tile_place";
     case MSDA_KERNEL_TILE_ACCUM: return "tile_accum";
+    case MSDA_KERNEL_TOUCH: return "touch_count";
     }
     return "unknown";
 }
@@ -851,12 +880,7 @@ size_t msda_backward_workspace_size(msda_dtype dt, msda_accum mode, int64_t B, i
     if (dt != MSDA_F16 && dt != MSDA_BF16) return 0;
     const msda_accum acc = msda_resolve_accum(dt, mode, B, S, M, D, L, K, Q);
     if (acc != MSDA_ACCUM_FP32) return 0;
-    Dims d{B, S, M, D, L, K, Q, 0, 0, 0};
-    TileLayout tl;
-    if (L >= 0 && K >= 0 && check_dims(dt, d) == MSDA_OK && tiled_layout(dt, acc, d, false, &tl)) return tl.bytes;
-    int64_t n;
-    if (!mul_ok(B, S, &n) || !mul_ok(n, M, &n) || !mul_ok(n, D, &n) || !mul_ok(n, 4, &n)) return SIZE_MAX;
-    return (size_t)n;
+    return msda::fp32_workspace_bytes(dt, B, S, M, D, L, K, Q, true);
 }
 
 }  // extern "C"
@@ -1115,17 +1139,59 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // and the rounding pass afterwards handles the remaining rows only.
     constexpr int kFoldLevel = 2;
     constexpr long long kFoldChunk = 1 << 16;   // workspace elements per folding block
-    const bool fold = passes > 1 && use_ws && d.L > kFoldLevel && pl.spec && fz == nullptr &&
-                      aligned(grad_value, 16) && (d.S * d.M * d.D) % 8 == 0;
+    // rounding by the tail kernel (msda_convert_tail_kernel): one pass per level,
+    // 16-byte aligned grad_value, whole 8-element groups
+    const bool tail_ok = passes > 1 && use_ws && pl.spec && fz == nullptr && aligned(grad_value, 16) &&
+                         (d.S * d.M * d.D) % 8 == 0;
+    // Touch classes (msda_device.cuh, touch_sparse): a count pass first classes
+    // the rows of the sparse levels; a row with one contribution is then
+    // written directly and the rounding reads the workspace rows with several
+    // only.  Needs the classes' bytes after the fp32 sums
+    // (msda_backward_workspace_size counts them); a workspace of the sums
+    // alone runs without.
+    const int tau = tune().tau > 0 ? tune().tau : kTouchTau;
+    const size_t map_off = touch_map_offset(d.n_value), map_bytes = touch_map_bytes(d.B, d.S, d.M);
+    const bool touch = tail_ok && !accumulate && tune().touch != 0 && 4 * d.Q * d.K <= (int64_t)tau * d.S &&
+                       d.B * d.S * d.M < (1ll << 31) && d.n_param < (1ll << 31) && d.D % 8 == 0 &&
+                       workspace_bytes >= map_off + map_bytes;
+    unsigned* touch_map = touch ? reinterpret_cast<unsigned*>(static_cast<unsigned char*>(workspace) + map_off)
+                                : nullptr;
+    // With the rounding folded into the passes from level 2 on, the rows below
+    // level 2's first row, final once passes 0 and 1 are done, are rounded by
+    // extra blocks of those passes, and the tail kernel rounds the rest.  Not
+    // with the touch classes by default: the passes of the coarse levels are
+    // bound by their own sampling (long-scoreboard waits on the L2), and the
+    // folding blocks, which then read few workspace rows, only take their slots.
+    const int tf = tune().fold;
+    const bool fold = tail_ok && d.L > kFoldLevel && (tf > 0 || (tf < 0 && !touch));
     long long fold_chunks = 0;
-    if (fold) {
-        a.conv_level = kFoldLevel;
+    if (fold || touch) {
+        a.conv_level = fold ? kFoldLevel : -1;   // -1: the tail kernel rounds every row
         a.conv_rezero = ws_zeroed ? 1 : 0;
         a.conv_out = grad_value;
         a.n_images = (int)d.B;
+    }
+    if (fold) {
         a.conv_chunk = kFoldChunk;
         a.conv_chunks_per_image = (a.slice + kFoldChunk - 1) / kFoldChunk;
         fold_chunks = d.B * a.conv_chunks_per_image;
+    }
+    if (touch) {
+        a.touch = touch_map;
+        a.touch_tau = tau;
+        a.touch_out = grad_value;
+        a.div_lk = fast_div((uint32_t)(d.L * d.K));
+        a.div_d8 = fast_div((uint32_t)(d.D / 8));
+        // the first pass reads the classes before its griddepcontrol.wait
+        pl.pdl = false;
+        if (!ws_zeroed && (s = launch_zero(touch_map, (int64_t)map_bytes, di->sms, st))) return s;
+        TraceScope ts(st);
+        const int grid = (int)((d.n_param + msda::kBlockThreads - 1) / msda::kBlockThreads);
+        if (dt == MSDA_F16) msda::launch_touch_count<__half>(a, grid, st);
+        else msda::launch_touch_count<__nv_bfloat16>(a, grid, st);
+        ts.end(MSDA_KERNEL_TOUCH, d.n_param);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "touch count kernel launch");
     }
     for (int pass = 0; pass < passes; ++pass) {
         Plan lp = pl;
@@ -1163,8 +1229,9 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "backward kernel launch");
     }
-    if (use_ws && fold) {
-        // the rows from the first row of level 2 on, in every batch image
+    if (use_ws && (fold || touch)) {
+        // the rows from the first row of level 2 on (with the folded
+        // rounding), else every row, in every batch image
         TraceScope ts(st);
         const int grid = grid_for(d.n_value / 8 / 16 + 1, di->sms);
         if (dt == MSDA_F16) msda::launch_convert_tail<__half>(a, grid, st);
@@ -1172,6 +1239,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
         ts.end(MSDA_KERNEL_CONVERT, d.n_value);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
+        // a workspace that came in holding zeros leaves holding zeros
+        if (touch && ws_zeroed && (s = launch_zero(touch_map, (int64_t)map_bytes, di->sms, st))) return s;
         if (fz && a.rbuf_off < 0) return launch_ref_grad(dt, d, spatial_shapes, grad_sampling_locations, fz->grad_ref, st);
         return MSDA_OK;
     }

@@ -48,6 +48,7 @@ enum ParamMode : int { PARAMS_DIRECT = 0, PARAMS_SMEM_LD = 1, PARAMS_SMEM_BULK =
 // Device error bits (msda_device_errors).
 constexpr unsigned kErrBadLevel = 1u;
 constexpr unsigned kErrBulkTimeout = 2u;
+constexpr unsigned kErrTouch = 8u;   // a corner row the touch count missed (never expected)
 
 // n / d for 0 <= n < 2^31 by a multiply-high and a shift (Granlund and
 // Montgomery, "Division by invariant integers using multiplication", 1994:
@@ -86,6 +87,7 @@ struct KernelArgs {
     int M, D, L, K, LK;
     int n_units;           // B * Q * M (< 2^31)
     FastDiv div_qm, div_m, div_k;
+    FastDiv div_lk, div_d8;  // by L*K and by D/8 (touch classes only)
     int lc, lp;            // log2(C), log2(P)
     int nvec;              // vectors per D-row
     int tpb;               // units (teams) per block
@@ -111,6 +113,15 @@ struct KernelArgs {
     long long conv_first, conv_chunk, conv_chunks_per_image;
     void* conv_out;
     int n_images;          // B
+    // Touch classes of the FP32 workspace's rows (see touch_sparse): 2 bits
+    // per (b, pixel, head) row, 16 rows a word, at (b*M + m)*S + pixel;
+    // class 0 no contribution, 1 exactly one, 2 (or 3) several.  A row of a
+    // sparse level with one contribution is written to touch_out (grad_value)
+    // directly and never reaches the workspace; rounding skips it, and writes
+    // zeros for an untouched one without reading the workspace.  NULL: off.
+    unsigned* touch;
+    int touch_tau;
+    void* touch_out;
 };
 
 // Head of the deterministic accumulator's workspace (256 bytes, then the
@@ -336,6 +347,23 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return done;
 }
 
+// Level l of the table: its sizes pass the check (1 <= H, W <= kMaxSide, the
+// level inside the S rows) or it has no corner inside (ok = 0).
+__device__ __forceinline__ Level level_of(const KernelArgs& a, int l) {
+    const long long H = a.shapes[2 * l], W = a.shapes[2 * l + 1], st = a.starts[l];
+    const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S && H * W <= a.S - st;
+    const long long MD = (long long)a.M * a.D;
+    Level v;
+    v.start_md = ok ? st * MD : 0;
+    v.w_md = ok ? W * MD : 0;
+    v.fH = ok ? (float)H : 0.f;
+    v.fW = ok ? (float)W : 0.f;
+    v.ok = ok;
+    v.W = ok ? (int)W : 0;
+    v.start = ok ? st : 0;
+    return v;
+}
+
 // Byte offset of the attention-weight chunk in the staged parameters.
 template <typename T>
 __device__ __forceinline__ int attn_chunk_offset(const KernelArgs& a) {
@@ -387,20 +415,8 @@ __device__ __forceinline__ bool prologue(const KernelArgs& a, Level* lv, unsigne
         for (int i = tid; i < nu * a.LK; i += blockDim.x) d2[i] = __ldg(s2 + i);
     }
     if (tid < a.L) {
-        const long long H = a.shapes[2 * tid], W = a.shapes[2 * tid + 1], st = a.starts[tid];
-        const bool ok = H >= 1 && W >= 1 && H <= kMaxSide && W <= kMaxSide && st >= 0 && st <= a.S &&
-                        H * W <= a.S - st;
-        const long long MD = (long long)a.M * a.D;
-        Level v;
-        v.start_md = ok ? st * MD : 0;
-        v.w_md = ok ? W * MD : 0;
-        v.fH = ok ? (float)H : 0.f;
-        v.fW = ok ? (float)W : 0.f;
-        v.ok = ok;
-        v.W = ok ? (int)W : 0;
-        v.start = ok ? st : 0;
-        lv[tid] = v;
-        if (!ok) atomicOr(a.err, kErrBadLevel);
+        lv[tid] = level_of(a, tid);
+        if (!lv[tid].ok) atomicOr(a.err, kErrBadLevel);
     }
     if (a.param_mode == PARAMS_SMEM_BULK && tid == 0) {
         uint32_t done = 0;
@@ -745,6 +761,7 @@ struct SampleSetup {
     int wmd;        // W * M * D of the sample's level
     unsigned mask;  // bit k: corner k inside the level
     float lx, ly;   // fractional offsets in the cell
+    int pix;        // pyramid row (pixel) of corner (y0, x0); not carried by shfl_setup
 };
 
 __device__ __forceinline__ SampleSetup sample_setup(const Level& L, float x, float y, int MD) {
@@ -765,6 +782,7 @@ __device__ __forceinline__ SampleSetup sample_setup(const Level& L, float x, flo
              ((unsigned)(vy1 && vx1) << 3);
     r.lx = xi - x0f;
     r.ly = yi - y0f;
+    r.pix = (int)L.start + y0 * L.W + x0;
     return r;
 }
 
@@ -775,6 +793,7 @@ __device__ __forceinline__ SampleSetup shfl_setup(const SampleSetup& s, int src)
     r.mask = __shfl_sync(0xffffffffu, s.mask, src);
     r.lx = __shfl_sync(0xffffffffu, s.lx, src);
     r.ly = __shfl_sync(0xffffffffu, s.ly, src);
+    r.pix = 0;
     return r;
 }
 
@@ -978,6 +997,114 @@ __global__ void __launch_bounds__(kBlockThreads) msda_fwd4_kernel(const KernelAr
     }
 }
 
+// ---------------------------------------------------------------------------
+// Touch classes of the FP32 workspace's rows (course ch. 5, "The fix:
+// accumulate in FP32, downcast at the end": the sum of one contribution,
+// rounded once, is that contribution rounded once).
+//
+// A level is sparse when its rows take few corner contributions: the 4*Q*K
+// corners of one (b, m) image over its H*W rows, at most touch_tau a row on
+// average.  For the large levels of a big pyramid most touched rows then
+// take exactly one contribution (for uniformly spread samples a fraction
+// e^-r of the rows is untouched and r*e^-r touched once, r = 4QK/HW), and
+// going through the workspace costs such a row a line fetch, a write-back
+// and a read by the rounding, where writing it directly costs one store.
+// A count pass before the sampling passes gives every row of the sparse
+// levels its class (0, 1 or 2 = several); the sampling pass then stores a
+// class-1 row's contribution to grad_value, rounded once, and reduces the
+// others into the workspace; rounding skips class-1 rows and writes zeros
+// for class-0 rows without reading the workspace.
+
+__device__ __forceinline__ bool touch_sparse(const KernelArgs& a, const Level& L) {
+    return L.ok && 4ll * a.Q * a.K <= (long long)a.touch_tau * (long long)L.fH * (long long)L.W;
+}
+
+// Class index of (image b, pixel, head m): (b*M + m)*S + pixel (< 2^31, host
+// check), head-major so that horizontally adjacent corners are adjacent
+// classes, mostly in one word.
+__device__ __forceinline__ unsigned touch_row(const KernelArgs& a, uint32_t b, int pix, uint32_t m) {
+    return ((unsigned)b * (unsigned)a.M + m) * (unsigned)a.S + (unsigned)pix;
+}
+
+__device__ __forceinline__ unsigned touch_bits(unsigned word, unsigned row) { return (word >> ((row & 15u) * 2u)) & 3u; }
+
+// grad_value[p..p+3] = (a, b, c, d), rounded once (8-byte aligned p)
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d) {
+    const T* tag = nullptr;
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack2(a, b, tag), pack2(c, d, tag));
+}
+
+// The count pass: one thread per sample (samples of dense levels return at
+// once).  A corner row's low bit is set by an atomic OR; a row whose low bit
+// was already set gets the high bit too.  The four ORs of a sample are
+// issued before any of their old values is used.  The bilinear setup is
+// sample_setup's, as in the sampling pass, so both see the same corners.
+template <typename T>
+__global__ void __launch_bounds__(kBlockThreads) msda_touch_count_kernel(const KernelArgs a) {
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    __shared__ int sparse[MSDA_MAX_LEVELS];
+    if (threadIdx.x < a.L) {
+        lv[threadIdx.x] = level_of(a, threadIdx.x);
+        sparse[threadIdx.x] = touch_sparse(a, lv[threadIdx.x]);
+    }
+    __syncthreads();
+    const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (uint32_t)a.n_units * (uint32_t)a.LK) return;
+    const uint32_t u = fdiv(i, a.div_lk);
+    const int s = (int)(i - u * (uint32_t)a.LK);
+    const int l = (int)fdiv((uint32_t)s, a.div_k);
+    if (!sparse[l]) return;
+    const T* pl = reinterpret_cast<const T*>(a.loc) + 2ll * i;
+    const SampleSetup st = sample_setup(lv[l], ldg_f(pl), ldg_f(pl + 1), a.M * a.D);
+    if (!st.mask) return;
+    const uint32_t b = fdiv(u, a.div_qm);
+    const uint32_t m = u - fdiv(u, a.div_m) * (uint32_t)a.M;
+    // corners (0, 1) and (2, 3) are adjacent classes: one OR per word
+    const unsigned r0 = touch_row(a, b, st.pix, m), r2 = r0 + (unsigned)lv[l].W;
+    const unsigned rows[4] = {r0, r0 + 1u, r2, r2 + 1u};
+    unsigned* w[4];
+    unsigned bit[4], old[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        w[k] = a.touch + (rows[k] >> 4);
+        bit[k] = ((st.mask >> k) & 1u) << ((rows[k] & 15u) * 2u);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; k += 2)
+        if (w[k] == w[k + 1]) {   // the pair in one word
+            bit[k] |= bit[k + 1];
+            bit[k + 1] = 0u;
+        }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) old[k] = bit[k] ? atomicOr(w[k], bit[k]) : 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (old[k] & bit[k]) atomicOr(w[k], (old[k] & bit[k]) << 1);
+}
+
+// Row ranges [begin, end) of the sparse levels in one image's rows
+// (pixel * M + m), in shared memory for the rounding kernels.
+struct TouchRanges {
+    unsigned begin[MSDA_MAX_LEVELS], end[MSDA_MAX_LEVELS];
+    int n;
+};
+
+__device__ __forceinline__ void touch_ranges(const KernelArgs& a, TouchRanges* r) {
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int l = 0; l < a.L; ++l) {
+            const Level v = level_of(a, l);
+            if (!touch_sparse(a, v)) continue;
+            r->begin[n] = (unsigned)v.start * (unsigned)a.M;
+            r->end[n] = (unsigned)(v.start + (long long)v.fH * v.W) * (unsigned)a.M;
+            ++n;
+        }
+        r->n = n;
+    }
+    __syncthreads();
+}
+
 // Eight workspace elements from index 8*i: rounded once into grad_value; with
 // rezero, the 32 bytes written back as zeros when any of them is non-zero.
 template <typename T>
@@ -1010,18 +1137,48 @@ __device__ __forceinline__ long long first_row_from(const KernelArgs& a, int l0)
     return p;
 }
 
+// round8 under the touch classes: group i (eight elements) of image img.  A
+// row of a sparse level with one contribution already holds it in grad_value;
+// one with none gets zeros, its workspace row unread.
+template <typename T>
+__device__ __forceinline__ void round8_touch(const KernelArgs& a, const TouchRanges& tr, float* ws, T* gv,
+                                             long long i, unsigned img) {
+    static_assert(sizeof(T) == 2, "eight 16-bit elements are one 16-byte store");
+    const unsigned row = fdiv((uint32_t)i, a.div_d8);
+    bool sp = false;
+    for (int j = 0; j < tr.n; ++j) sp |= row >= tr.begin[j] && row < tr.end[j];
+    if (sp) {
+        const unsigned pix = fdiv(row, a.div_m);
+        const unsigned id = (img * (unsigned)a.M + (row - pix * (unsigned)a.M)) * (unsigned)a.S + pix;
+        const unsigned c = touch_bits(__ldg(a.touch + (id >> 4)), id);
+        if (c == 1u) return;
+        if (c == 0u) {
+            *reinterpret_cast<uint4*>(gv + 8 * i) = make_uint4(0u, 0u, 0u, 0u);
+            return;
+        }
+    }
+    round8<T>(ws, gv, i, a.conv_rezero);
+}
+
 // One folded chunk: workspace elements [k*conv_chunk, (k+1)*conv_chunk) of
 // batch image img, cut at the first row of the levels >= conv_level.
 template <typename T>
 __device__ __noinline__ void fold_round_chunk(const KernelArgs& a, long long c) {
     __shared__ long long cut;
+    __shared__ TouchRanges tr;
     if (threadIdx.x == 0) cut = first_row_from(a, a.conv_level) * a.M * a.D;
-    __syncthreads();
+    if (a.touch) touch_ranges(a, &tr);
+    else __syncthreads();
     const long long img = c / a.conv_chunks_per_image, k = c - img * a.conv_chunks_per_image;
     const long long e0 = k * a.conv_chunk, e1 = min(e0 + a.conv_chunk, cut);
     float* ws = reinterpret_cast<float*>(a.grad_acc) + img * a.slice;
     T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
-    for (long long i = e0 / 8 + threadIdx.x; i < e1 / 8; i += blockDim.x) round8<T>(ws, gv, i, a.conv_rezero);
+    if (a.touch) {
+        for (long long i = e0 / 8 + threadIdx.x; i < e1 / 8; i += blockDim.x)
+            round8_touch<T>(a, tr, ws, gv, i, (unsigned)img);
+    } else {
+        for (long long i = e0 / 8 + threadIdx.x; i < e1 / 8; i += blockDim.x) round8<T>(ws, gv, i, a.conv_rezero);
+    }
 }
 
 // Backward, same decomposition.  Each round first gathers the corners of its
@@ -1037,7 +1194,7 @@ constexpr int kMergeCells = 1;
 constexpr int kMergeCorners = 2;
 constexpr int kGatherOnly = -1;
 
-template <typename T, typename ACC, int NV, bool FUSED, int MERGE>
+template <typename T, typename ACC, int NV, bool FUSED, int MERGE, bool TOUCH>
 __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
     constexpr int EPV = 16 / sizeof(T);
     constexpr int JB = kGatherBatchBwd;
@@ -1084,6 +1241,10 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
     const T* vbase = reinterpret_cast<const T*>(a.value) + vofs;
     ACC* gbase = reinterpret_cast<ACC*>(a.grad_acc) + vofs;
     const int MD = a.M * a.D;
+    // TOUCH: the touch classes (FP32 workspace, 16-bit I/O, no merge): a
+    // sparse level's rows with one contribution are written directly
+    static_assert(!TOUCH || (SPLIT && !FUSED && MERGE == 0), "touch classes: FP32 workspace, unfused, no merge");
+    T* tbase = TOUCH ? reinterpret_cast<T*>(a.touch_out) + vofs : nullptr;
     auto load_raw = [&](const T* p) -> typename S_::Raw {
         if constexpr (SPLIT) return split_load_raw(p);
         else return S_::load_raw(p);
@@ -1146,6 +1307,20 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
             }
         }
         const SampleSetup me = sample_setup(lev, x, y, MD);
+        // touch words of this lane's sample's corner rows, loaded now and
+        // read after the gather (sparse levels only; else every corner is
+        // reduced into the workspace)
+        unsigned tw[4] = {0u, 0u, 0u, 0u};
+        bool tsp = false;
+        if constexpr (TOUCH) {
+            tsp = live && touch_sparse(a, lev);
+            if (tsp) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if ((me.mask >> k) & 1u)
+                        tw[k] = __ldg(a.touch + (touch_row(a, b, me.pix + (k & 1) + (k >> 1) * lev.W, m) >> 4));
+            }
+        }
 
         // gather + reduce: the lane with c == j keeps the totals of sample j
         float ra = 0.f, rx = 0.f, ry = 0.f;
@@ -1297,6 +1472,26 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
                 }
             }
 
+            // the sample's corner classes, 2 bits each (2 = reduce into the workspace)
+            unsigned tcls = 0xAAu;
+            if constexpr (TOUCH) {
+                if (tsp) {
+                    tcls = 0u;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        unsigned c = 2u;
+                        if ((me.mask >> k) & 1u) {
+                            c = touch_bits(tw[k], touch_row(a, b, me.pix + (k & 1) + (k >> 1) * lev.W, m));
+                            if (c == 0u) {   // the count pass missed it: never expected
+                                atomicOr(a.err, kErrTouch);
+                                c = 2u;
+                            }
+                        }
+                        tcls |= c << (2 * k);
+                    }
+                }
+            }
+
             // scatter: A * w_corner * g into the inside corners
             if (!waited) {
                 asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1309,6 +1504,7 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
                 const int so = __shfl_sync(0xffffffffu, me.o, src);
                 const int swmd = __shfl_sync(0xffffffffu, me.wmd, src);
                 const unsigned smk = __shfl_sync(0xffffffffu, smask, src);
+                const unsigned scls = TOUCH ? __shfl_sync(0xffffffffu, tcls, src) : 0xAAu;
                 float cj[4];
     #pragma unroll
                 for (int k = 0; k < 4; ++k) cj[k] = __shfl_sync(0xffffffffu, mc[k], src);
@@ -1333,9 +1529,16 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
                                 t[e + 1] = r.y;
                             }
                             if constexpr (SPLIT) {
-                                float* q = gbase + off[k] + n * kC * EPV;
-                                red_v4_f32(q, t[0], t[1], t[2], t[3]);
-                                red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+                                if (TOUCH && ((scls >> (2 * k)) & 3u) == 1u) {
+                                    // the row's one contribution, rounded once
+                                    T* q = tbase + off[k] + n * kC * EPV;
+                                    store4<T>(q, t[0], t[1], t[2], t[3]);
+                                    store4<T>(q + 16, t[4], t[5], t[6], t[7]);
+                                } else {
+                                    float* q = gbase + off[k] + n * kC * EPV;
+                                    red_v4_f32(q, t[0], t[1], t[2], t[3]);
+                                    red_v4_f32(q + 16, t[4], t[5], t[6], t[7]);
+                                }
                             } else {
                                 Scatter<ACC, EPV>::add(gbase + off[k] + n * kC * EPV, t);
                             }
@@ -1377,9 +1580,9 @@ __device__ __forceinline__ void bwd4_body(const KernelArgs& a) {
     }
 }
 
-template <typename T, typename ACC, int NV, bool FUSED, int MERGE>
+template <typename T, typename ACC, int NV, bool FUSED, int MERGE, bool TOUCH = false>
 __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelArgs a) {
-    bwd4_body<T, ACC, NV, FUSED, MERGE>(a);
+    bwd4_body<T, ACC, NV, FUSED, MERGE, TOUCH>(a);
 }
 
 // The merging backward for one slot per lane, held to four resident blocks
@@ -1388,7 +1591,7 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd4_kernel(const KernelAr
 // of the merge gains (344 us at three blocks, 306 us at four).
 template <typename T, typename ACC, bool FUSED, int MERGE>
 __global__ void __launch_bounds__(kBlockThreads, 4) msda_bwd4_merge1_kernel(const KernelArgs a) {
-    bwd4_body<T, ACC, 1, FUSED, MERGE>(a);
+    bwd4_body<T, ACC, 1, FUSED, MERGE, false>(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -1745,19 +1948,81 @@ __global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, 
 
 // The rounding pass for the rows the backward passes did not round
 // themselves: in every batch image, the rows from the first row of the levels
-// >= a.conv_level on (16-byte aligned workspace and grad_value, slices of a
-// multiple of 8 elements).
+// >= a.conv_level on, every row with a.conv_level < 0 (16-byte aligned
+// workspace and grad_value, slices of a multiple of 8 elements).
 template <typename T>
 __global__ void __launch_bounds__(kBlockThreads) msda_convert_tail_kernel(const KernelArgs a) {
+    static_assert(sizeof(T) == 2, "eight 16-bit elements are one 16-byte store");
     __shared__ long long cut;
-    if (threadIdx.x == 0) cut = first_row_from(a, a.conv_level) * a.M * a.D;
-    __syncthreads();
+    __shared__ TouchRanges tr;
+    if (threadIdx.x == 0) cut = a.conv_level < 0 ? 0 : first_row_from(a, a.conv_level) * a.M * a.D;
+    if (a.touch) touch_ranges(a, &tr);
+    else __syncthreads();
+    // U groups of eight elements a thread in flight: their touch words are
+    // loaded together, then the workspace rows they need, then the stores
+    constexpr int U = 4;
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nth = (long long)gridDim.x * blockDim.x;
+    const long long n8 = a.slice / 8;
     for (int img = 0; img < a.n_images; ++img) {
-        float* ws = reinterpret_cast<float*>(a.grad_acc) + img * a.slice;
+        const float4* ws = reinterpret_cast<const float4*>(reinterpret_cast<float*>(a.grad_acc) + img * a.slice);
+        float4* wz = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.grad_acc) + img * a.slice);
         T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
-        for (long long i = cut / 8 + tid; i < a.slice / 8; i += nth) round8<T>(ws, gv, i, a.conv_rezero);
+        for (long long i0 = cut / 8 + tid; i0 < n8; i0 += U * nth) {
+            // class of each group's row: 0 untouched, 1 written by the sampling
+            // pass, 2 reduced into the workspace (every row of a dense level)
+            unsigned cls[U], id[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const long long i = i0 + u * nth;
+                cls[u] = i < n8 ? 2u : 4u;   // 4: past the end
+                id[u] = 0u;
+                if (a.touch && i < n8) {
+                    const unsigned row = fdiv((uint32_t)i, a.div_d8);
+                    bool sp = false;
+                    for (int j = 0; j < tr.n; ++j) sp |= row >= tr.begin[j] && row < tr.end[j];
+                    if (sp) {
+                        const unsigned pix = fdiv(row, a.div_m);
+                        id[u] = ((unsigned)img * (unsigned)a.M + (row - pix * (unsigned)a.M)) * (unsigned)a.S + pix;
+                        cls[u] = 3u;   // sparse: from its touch word below
+                    }
+                }
+            }
+            unsigned w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) w[u] = cls[u] == 3u ? __ldg(a.touch + (id[u] >> 4)) : 0u;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (cls[u] == 3u) cls[u] = min(touch_bits(w[u], id[u]), 2u);
+            float4 x[U], y[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const long long i = i0 + u * nth;
+                if (cls[u] == 2u) {
+                    x[u] = __ldcs(ws + 2 * i);
+                    y[u] = __ldcs(ws + 2 * i + 1);
+                } else {
+                    x[u] = y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const long long i = i0 + u * nth;
+                if (cls[u] == 0u || cls[u] == 2u) {
+                    const float f[8] = {x[u].x, x[u].y, x[u].z, x[u].w, y[u].x, y[u].y, y[u].z, y[u].w};
+                    Slot<T, 8>::store(gv + 8 * i, f);
+                }
+                if (cls[u] == 2u && a.conv_rezero) {
+                    const uint32_t nz = __float_as_uint(x[u].x) | __float_as_uint(x[u].y) | __float_as_uint(x[u].z) |
+                                        __float_as_uint(x[u].w) | __float_as_uint(y[u].x) | __float_as_uint(y[u].y) |
+                                        __float_as_uint(y[u].z) | __float_as_uint(y[u].w);
+                    if (nz) {
+                        __stcs(wz + 2 * i, make_float4(0.f, 0.f, 0.f, 0.f));
+                        __stcs(wz + 2 * i + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+                    }
+                }
+            }
+        }
     }
 }
 

@@ -87,6 +87,14 @@ static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     // workspace, whole cells otherwise (the faster of the two on GB300 for
     // each accumulator)
     constexpr int MODE = (std::is_same<ACC, float>::value && sizeof(T) == 2) ? kMergeCorners : kMergeCells;
+    if constexpr (std::is_same<ACC, float>::value && sizeof(T) == 2 && !FUSED) {
+        // the touch classes of the workspace rows: their own kernel (its
+        // extra registers stay out of the others), without the corner merge
+        if (a.touch) {
+            launch_plan(msda_bwd4_kernel<T, ACC, NV, false, 0, true>, a, pl, st);
+            return;
+        }
+    }
     if (!pl.merge) {
         launch_plan(msda_bwd4_kernel<T, ACC, NV, FUSED, 0>, a, pl, st);
     } else {
@@ -185,6 +193,11 @@ void launch_convert_tail(const KernelArgs& a, int grid, cudaStream_t st) {
 }
 
 template <typename T>
+void launch_touch_count(const KernelArgs& a, int grid, cudaStream_t st) {
+    msda_touch_count_kernel<T><<<grid, kBlockThreads, 0, st>>>(a);
+}
+
+template <typename T>
 void launch_widen(const T* gv, float* ws, long long n, int grid, cudaStream_t st) {
     msda_widen_kernel<T><<<grid, kBlockThreads, 0, st>>>(gv, ws, n);
 }
@@ -254,7 +267,8 @@ MSDA_EXTERN_IO(__nv_bfloat16)
     extern template void launch_backward<T, T>(const KernelArgs&, const Plan&, cudaStream_t);           \
     extern template void launch_convert<T>(float*, T*, long long, int, int, int, cudaStream_t);         \
     extern template void launch_widen<T>(const T*, float*, long long, int, cudaStream_t);                \
-    extern template void launch_convert_tail<T>(const KernelArgs&, int, cudaStream_t);
+    extern template void launch_convert_tail<T>(const KernelArgs&, int, cudaStream_t);            \
+    extern template void launch_touch_count<T>(const KernelArgs&, int, cudaStream_t);
 MSDA_EXTERN_HALF(__half)
 MSDA_EXTERN_HALF(__nv_bfloat16)
 #undef MSDA_EXTERN_HALF

@@ -7,9 +7,9 @@
 // engine plugin whose enqueue hook receives pointers but no allocator, a
 // real-time loop that forbids allocation after start-up, or code enqueuing
 // work under a memory budget fixed by someone else.  msda_backward with the
-// FP32 accumulator needs msda_backward_workspace_size(dt, MSDA_ACCUM_FP32,
-// ...) bytes of scratch; here that scratch is the array below, sized at
-// compile time.
+// FP32 accumulator needs B*S*M*D*4 bytes of scratch for its fp32 sums (plus
+// the optional touch classes of their rows); here that scratch is the array
+// below, sized at compile time.
 //
 // The array is a device global of this translation unit's module: it
 // occupies MSDA_STATIC_WORKSPACE_BYTES on every device where that module is
@@ -90,11 +90,12 @@ extern "C" msda_status msda_backward_static_workspace(
                                   level_start_index, sampling_locations, attention_weights, grad_out, grad_value,
                                   grad_sampling_locations, grad_attention_weights, nullptr, 0, stream);
     if (s != MSDA_ERR_WORKSPACE) return s;
-    const size_t need = msda_backward_workspace_size(dt, MSDA_ACCUM_FP32, B, S, M, D, L, K, Q);
+    // the fp32 sums must fit; the touch classes are used when they fit too
+    const size_t need = msda::fp32_workspace_bytes(dt, B, S, M, D, L, K, Q, false);
     if (need > (size_t)MSDA_STATIC_WORKSPACE_BYTES)
         return msda::set_error(MSDA_ERR_WORKSPACE,
                                "msda_backward_static_workspace: the FP32 accumulator needs more scratch than the "
-                               "static workspace holds (msda_backward_workspace_size > MSDA_STATIC_WORKSPACE_BYTES)");
+                               "static workspace holds (B*S*M*D*4 > MSDA_STATIC_WORKSPACE_BYTES)");
     void* ws = nullptr;
     s = static_workspace_address(reinterpret_cast<cudaStream_t>(stream), &ws);
     if (s != MSDA_OK) return s;

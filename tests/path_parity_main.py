@@ -25,9 +25,17 @@ def main():
         ("bf16", 32, 4, "fp32"), ("f16", 32, 4, "native"), ("f32", 16, 4, "auto"),
         ("bf16", 128, 4, "native"), ("f16", 128, 2, "fp32"), ("f32", 64, 4, "auto"),
     ]
-    for dtype, D, K, accum in cases:
-        wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, D=D, K=K, B=2, Q=41, M=3,
-                                               shapes=((11, 13), (6, 7), (3, 5), (2, 2)))
+    small = ((11, 13), (6, 7), (3, 5), (2, 2))
+    # a pyramid whose large levels take few samples a row: 4*Q*K = 656 corners
+    # over 3072, 768, 192 and 48 rows a head (the touch classes of the FP32
+    # workspace's rows find untouched, once- and several-times-touched rows)
+    sparse = ((48, 64), (24, 32), (12, 16), (6, 8))
+    cases = [c + (small,) for c in cases] + [
+        ("bf16", 32, 4, "fp32", sparse), ("f16", 64, 4, "fp32", sparse), ("bf16", 96, 4, "fp32", sparse),
+        ("f16", 128, 4, "fp32", sparse), ("bf16", 32, 4, "native", sparse),
+    ]
+    for dtype, D, K, accum, shapes in cases:
+        wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, D=D, K=K, B=2, Q=41, M=3, shapes=shapes)
         inp = W.make_inputs(wl)
         t = to_torch(inp, dtype, "cuda:0")
         out = msda.forward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
@@ -35,7 +43,7 @@ def main():
         gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
                                    t["attention_weights"], t["grad_out"], accum=accum)
         torch.cuda.synchronize()
-        what = f"{os.environ.get('MSDA_TUNE')} {dtype} D={D} K={K}"
+        what = f"{os.environ.get('MSDA_TUNE')} {dtype} D={D} K={K} {accum} S={wl.S}"
         assert_forward(dtype, f64(out), oracle.forward(inp, dtype), what)
         rgv, rgl, rga = oracle.backward(inp, dtype)
         assert_grad(dtype, f64(gv), rgv, what + " grad_value")

@@ -5,7 +5,8 @@ parameter loads, the staged loads without the bulk copy, the backward's
 corner merge forced on and off, ordinary (non-programmatic) launches, and
 the FP32 accumulator on chip forced on (with tiles of 16 rows: most points
 straddle tiles) and off, and the backward run one pass per level (with and
-without the corner merge) or in one pass.  Each runs in a
+without the corner merge, with the touch classes of the FP32 workspace's
+rows off, and with every level or no level sparse) or in one pass.  Each runs in a
 child process with MSDA_TUNE set."""
 import os
 import subprocess
@@ -19,7 +20,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 @pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel",
                                   "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled",
-                                  "levelpass", "levelpass,merge", "nolevelpass", "levelpass,nomerge"])
+                                  "levelpass", "levelpass,merge", "nolevelpass", "levelpass,nomerge",
+                                  "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():

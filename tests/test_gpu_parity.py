@@ -437,16 +437,21 @@ def test_workspace_zeroed_flag(dtype, accumulate):
         assert int(torch.count_nonzero(ws)) == 0, "the workspace must hold zeros after the call"
 
 
-@pytest.mark.parametrize("levels_reversed,zeroed", [(False, False), (True, False), (False, True)])
-def test_level_passes_round_finished_rows(levels_reversed, zeroed):
+@pytest.mark.parametrize("levels_reversed,zeroed,big0", [(False, False, False), (True, False, False),
+                                                          (False, True, False), (False, False, True),
+                                                          (True, True, True)])
+def test_level_passes_round_finished_rows(levels_reversed, zeroed, big0):
     """A problem large enough for one backward pass per level (the fp32
     workspace exceeds the L2, and there are many units): the passes of the
     coarse levels round the workspace rows below the first row of level 2.
     With the levels stored in reverse order in the pyramid that cut is row 0,
-    so every row is left to the rounding pass.  Both against the oracle, with
-    and without a workspace that holds zeros on entry (and must on return)."""
+    so every row is left to the rounding pass.  Level 0 is sparse (3.7
+    corners a row and head; 0.9 with big0, where most of its rows take none
+    or one): its rows with one contribution are written directly.  Against
+    the oracle, with and without a workspace that holds zeros on entry (and
+    must on return)."""
     msda = _msda()
-    shapes = ((256, 256), (128, 128), (64, 64), (32, 32))
+    shapes = ((512 if big0 else 256, 512 if big0 else 256), (128, 128), (64, 64), (32, 32))
     wl = W.WORKLOADS["decoder_bf16"].with_(B=2, Q=15000, shapes=shapes, seed=51)
     assert wl.B * wl.S * wl.M * wl.D * 4 > 160e6 and wl.units * 4 > 8 * 152 * 768
     inp = dict(W.make_inputs(wl))

@@ -53,9 +53,17 @@ def _call(f, dtype, flags, dims, t, gv, gl, ga):
 
 
 def _need(lib, dtype, dims):
+    """Scratch the static array must hold: the FP32 accumulator's fp32 sums,
+    B*S*M*D*4 bytes for fp16/bf16 I/O (the touch classes that
+    msda_backward_workspace_size adds are optional), none for fp32 I/O."""
     from scale_deformable_attention_gb300 import _lib
 
-    return int(lib.msda_backward_workspace_size(CODE[dtype], _lib.ACCUM["fp32"], *dims))
+    full = int(lib.msda_backward_workspace_size(CODE[dtype], _lib.ACCUM["fp32"], *dims))
+    if full == 0:
+        return 0
+    B, S, M, D = dims[:4]
+    assert full >= B * S * M * D * 4
+    return B * S * M * D * 4
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
