@@ -313,6 +313,22 @@ class GpuStep:
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in ev]
 
+    def timed_steps(self, steps: int):
+        """As timed(step), plus the backward's share of each step: a third
+        event between the forward and the backward.  Returns (step ms, backward
+        ms) per step."""
+        torch = self.torch
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+        for a, m, b in ev:
+            self.flush()
+            a.record()
+            self.forward()
+            m.record()
+            self.backward()
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, m, b in ev], [m.elapsed_time(b) for a, m, b in ev]
+
 
 def _dist(backend: str = "nccl"):
     import torch.distributed as dist
@@ -345,14 +361,16 @@ def job_throughput(units_per_rank: int, world: int, steps: int, total_ms: float)
     return units_per_rank * world * steps / (total_ms / 1e3)
 
 
-def unique_fractions(model: dict, kernels: dict, peak: float):
+def unique_fractions(model: dict, kernels: dict, peak: float, bwd_wall_ms: float = None):
     """Compulsory-byte (unique value rows) fractions of the measured peak for
     the traced forward and backward (every other kernel of the step: zero,
-    backward passes, convert) durations per step."""
+    backward passes, convert) durations per step; the backward's wall time
+    in the timed steps instead when given (its kernels may overlap on two
+    streams)."""
     if "forward_unique" not in model or "forward" not in kernels or "backward" not in kernels:
         return None
     tf = kernels["forward"]["ms_per_step"]
-    tb = sum(v["ms_per_step"] for k, v in kernels.items() if k != "forward")
+    tb = bwd_wall_ms or sum(v["ms_per_step"] for k, v in kernels.items() if k != "forward")
     return {"unique_rows": model["unique_rows"], "forward_bytes": model["forward_unique"],
             "backward_bytes": model["bwd_total_unique"],
             "forward_frac": round(model["forward_unique"] / (tf / 1e3) / 1e9 / peak, 4),
@@ -474,11 +492,14 @@ def traced_pass(st, steps: int):
     return recs, dropped
 
 
-def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2: int, kernels: dict):
+def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2: int, kernels: dict,
+                bwd_wall_ms: float = None):
     """The dominant kernel against the measured HBM peak: its algorithmic
     bytes per step (per-corner model) over its traced time per step, i.e. the
     per-launch ratio when it launches once per step, and the launch-weighted
-    one when it launches once per level."""
+    one when it launches once per level.  The FP32 accumulator's backward is
+    taken whole (its kernels overlap on two streams): over the wall time of
+    the backward call in the timed steps, `bwd_wall_ms`."""
     peak, peak_kind = peaks()
     k = dict(kernels[dom])
     name = dom
@@ -491,8 +512,13 @@ def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2
         name = "backward+convert"
         alg = model["backward"] + model["convert"]
         c = kernels["convert"]
-        k = {"avg_ms": None, "launches": k["launches"] + c["launches"], "steps": k.get("steps", 1),
-             "ms_per_step": round(k["ms_per_step"] + c["ms_per_step"], 5)}
+        t = kernels.get("touch_count", {"launches": 0, "ms_per_step": 0.0})
+        launches = k["launches"] + c["launches"] + t["launches"]
+        traced = k["ms_per_step"] + c["ms_per_step"] + t["ms_per_step"]
+        if "touch_count" in kernels:
+            alg += model["touch_count"]
+        k = {"avg_ms": None, "launches": launches, "steps": k.get("steps", 1),
+             "ms_per_step": round(bwd_wall_ms if bwd_wall_ms else traced, 5)}
     achieved = alg / (k["ms_per_step"] / 1e3) / 1e9
     roof = {"kernel": name, "bound": bound_of(dom, wl, accum, l2, "tile_accum" in per),
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -500,7 +526,10 @@ def roofline_of(dom: str, per: dict, wl: W.Workload, model: dict, accum: str, l2
             "algorithmic_bytes": alg, "bytes_model": "per-corner (every in-level corner row each time)",
             "avg_launch_ms": k["avg_ms"], "launches_per_step": round(k["launches"] / max(1, k.get("steps", 1)), 3),
             "ms_per_step": k["ms_per_step"], "peak_source": peak_kind, "launches_traced": k["launches"]}
-    uf = unique_fractions(model, kernels, peak)
+    if name == "backward+convert" and bwd_wall_ms:
+        roof["time_source"] = ("wall time of the backward call (every kernel from the touch count to the "
+                               "rounding, two streams) in the timed steps, CUDA events on the launching stream")
+    uf = unique_fractions(model, kernels, peak, bwd_wall_ms)
     if uf:
         roof["compulsory_frac"] = uf["backward_frac"] if dom != "forward" else uf["forward_frac"]
         roof["compulsory_scope"] = ("backward pass (every kernel after the forward)" if dom != "forward"
@@ -547,7 +576,7 @@ def run_ours(args):
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
     with ClockSampler(uuid) as clk:
-        times = st.timed(st.step, args.steps)
+        times, bwd_times = st.timed_steps(args.steps)
     torch.cuda.synchronize()
     total_ms = max_over_ranks(float(sum(times)), dist, device)
     ms_per_step = total_ms / args.steps
@@ -560,7 +589,7 @@ def run_ours(args):
     for v in kernels.values():
         v["steps"] = n_traced
     dom = max(per, key=lambda k: sum(per[k])) if per else None
-    roof = roofline_of(dom, per, wl, model, resolved, l2, kernels) if dom else None
+    roof = roofline_of(dom, per, wl, model, resolved, l2, kernels, statistics.mean(bwd_times)) if dom else None
     peak, _ = peaks()
 
     graph = graph_cross_check(st, min(args.steps, 2000)) if not args.no_graph else None
@@ -591,7 +620,8 @@ def run_ours(args):
             "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
             "roofline": roof, "kernels": kernels, "kernels_source": "separate traced pass after the timed steps",
             "bytes_per_step_model": model["step"],
-            "unique_model": unique_fractions(model, kernels, peak),
+            "unique_model": unique_fractions(model, kernels, peak, statistics.mean(bwd_times)),
+            "backward_wall_ms": round(statistics.mean(bwd_times), 5),
             "reduction_roofline": reduction_roofline(wl, corners, resolved, kernels, red_ceiling),
             "step_gbs_model": round(model["step"] / (ms_per_step / 1e3) / 1e9, 1),
             "e2e": e2e, "cpu_baseline": cpu, "trace_dropped": dropped, "graph_cross_check": graph,

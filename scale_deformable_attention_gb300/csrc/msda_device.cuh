@@ -110,6 +110,7 @@ struct KernelArgs {
     // below the first row of levels >= conv_level, which no pass from
     // conv_level on adds to.  conv_first: this launch's first chunk.
     int conv_blocks, conv_every, conv_level, conv_rezero;
+    int conv_below;        // tail rounding: the rows below that first row instead of from it on
     long long conv_first, conv_chunk, conv_chunks_per_image;
     void* conv_out;
     int n_images;          // B
@@ -1948,27 +1949,31 @@ __global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, 
 
 // The rounding pass for the rows the backward passes did not round
 // themselves: in every batch image, the rows from the first row of the levels
-// >= a.conv_level on, every row with a.conv_level < 0 (16-byte aligned
-// workspace and grad_value, slices of a multiple of 8 elements).
+// >= a.conv_level on (below it with a.conv_below), every row with
+// a.conv_level < 0 (16-byte aligned workspace and grad_value, slices of a
+// multiple of 8 elements).
 template <typename T>
-__global__ void __launch_bounds__(kBlockThreads) msda_convert_tail_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(kBlockThreads, 8) msda_convert_tail_kernel(const KernelArgs a) {
     static_assert(sizeof(T) == 2, "eight 16-bit elements are one 16-byte store");
     __shared__ long long cut;
     __shared__ TouchRanges tr;
     if (threadIdx.x == 0) cut = a.conv_level < 0 ? 0 : first_row_from(a, a.conv_level) * a.M * a.D;
     if (a.touch) touch_ranges(a, &tr);
     else __syncthreads();
+    const long long g0 = a.conv_below ? 0 : cut / 8, n8 = a.conv_below ? cut / 8 : a.slice / 8;
     // U groups of eight elements a thread in flight: their touch words are
-    // loaded together, then the workspace rows they need, then the stores
-    constexpr int U = 4;
+    // loaded together, then the workspace rows they need, then the stores.
+    // Measured on GB300 (stress rounding, 8.6 GB of workspace): U = 2 at
+    // eight blocks an SM 1.47 ms; U = 4 (57 registers, four blocks) 1.53 ms,
+    // U = 2 at four blocks 1.75 ms, U = 8 1.92 ms.
+    constexpr int U = 2;
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long nth = (long long)gridDim.x * blockDim.x;
-    const long long n8 = a.slice / 8;
     for (int img = 0; img < a.n_images; ++img) {
         const float4* ws = reinterpret_cast<const float4*>(reinterpret_cast<float*>(a.grad_acc) + img * a.slice);
         float4* wz = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.grad_acc) + img * a.slice);
         T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
-        for (long long i0 = cut / 8 + tid; i0 < n8; i0 += U * nth) {
+        for (long long i0 = g0 + tid; i0 < n8; i0 += U * nth) {
             // class of each group's row: 0 untouched, 1 written by the sampling
             // pass, 2 reduced into the workspace (every row of a dense level)
             unsigned cls[U], id[U];

@@ -11,18 +11,27 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _inputs(dtype, seed):
-    wl = W.WORKLOADS["decoder_bf16"].with_(dtype=dtype, B=2, Q=120, seed=seed)
+# large enough for one backward pass per level, with a sparse level 0: the FP32
+# accumulator then counts touch classes and rounds on a second stream, which
+# the capture forks and joins
+_BIG = dict(Q=15000, shapes=((256, 256), (128, 128), (64, 64), (32, 32)))
+
+
+def _inputs(dtype, seed, big=False):
+    kw = dict(dtype=dtype, B=2, Q=120, seed=seed)
+    kw.update(_BIG if big else {})
+    wl = W.WORKLOADS["decoder_bf16"].with_(**kw)
     return wl, to_torch(W.make_inputs(wl), dtype, DEV)
 
 
-@pytest.mark.parametrize("dtype,accum", [("bf16", "native"), ("bf16", "fp32"), ("f32", "auto")])
-def test_graph_replay_matches_eager(dtype, accum):
+@pytest.mark.parametrize("dtype,accum,big", [("bf16", "native", False), ("bf16", "fp32", False), ("f32", "auto", False),
+                                             ("bf16", "fp32", True)])
+def test_graph_replay_matches_eager(dtype, accum, big):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import scale_deformable_attention_gb300 as msda
 
-    wl, t = _inputs(dtype, 31)
+    wl, t = _inputs(dtype, 31, big)
     bufs = {k: v.clone() for k, v in t.items()}
 
     def step():
@@ -46,7 +55,7 @@ def test_graph_replay_matches_eager(dtype, accum):
         captured = step()
 
     for seed in (32, 33):
-        _, fresh = _inputs(dtype, seed)
+        _, fresh = _inputs(dtype, seed, big)
         for k in bufs:
             bufs[k].copy_(fresh[k])
         g.replay()

@@ -21,7 +21,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 @pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel",
                                   "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled",
                                   "levelpass", "levelpass,merge", "nolevelpass", "levelpass,nomerge",
-                                  "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000"])
+                                  "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000", "levelpass,overlap"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
