@@ -155,7 +155,7 @@ int ilog2_floor(int v) {
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
 // params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
 // merge, nomerge, tiled, notiled, tp=<rows>, levelpass, nolevelpass, touch, notouch, tau=<n>, fold, nofold,
-// overlap, nooverlap.
+// overlap, nooverlap, nol2hint.
 // None of them changes results beyond the rounding order of the grad_value sums.
 
 struct Tune {
@@ -174,7 +174,7 @@ struct Tune {
     int tau = 0;           // sparse-level bound of the touch classes (tau=<n>; 0: the default)
     int fold = -1;         // rounding folded into the level passes: -1 unless the touch classes apply, 0 off (nofold), 1 on (fold)
     int overlap = -1;      // touch classes: rounding of the finished rows on a second stream: -1 default, 0 off (nooverlap), 1 on (overlap)
-    int ovgrid = 0;        // blocks an SM of that rounding (ovgrid=<n>; 0: as the tail's)
+    bool l2hint = true;    // TMA-gather forward: evict-first for levels over twice the L2 (off: nol2hint)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -209,7 +209,7 @@ const Tune& tune() {
             else if (!strcmp(tok, "fold")) r.fold = 1;
             else if (!strcmp(tok, "overlap")) r.overlap = 1;
             else if (!strcmp(tok, "nooverlap")) r.overlap = 0;
-            else if (!strncmp(tok, "ovgrid=", 7)) r.ovgrid = atoi(tok + 7);
+            else if (!strcmp(tok, "nol2hint")) r.l2hint = false;
         }
         return r;
     }();
@@ -818,6 +818,7 @@ msda_status forward_core(msda_dtype dt, const Dims& d, const void* value, const 
     } else if (tma) {
         a.lc = 2;
         a.lp = ilog2(LK / 4);
+        a.l2_bytes = tune().l2hint ? di->l2_bytes : 0;
         const int64_t groups = (d.units * LK + 31) / 32;
         const unsigned grid = (unsigned)((groups + msda::kTmaWarps - 1) / msda::kTmaWarps);
         switch (dt) {
@@ -1198,7 +1199,10 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // the tail kernel afterwards rounds the rest.  Measured on GB300, stress
     // backward: 4.67 -> 4.50 ms (the second stream's rounding at the tail
     // kernel's grid; at one, two or four blocks an SM it takes 7.0, 4.1 and
-    // 3.1 ms and the backward 8.9, 6.2 and 5.2 ms).
+    // 3.1 ms and the backward 8.9, 6.2 and 5.2 ms; the passes on a
+    // highest-priority stream and the rounding in short blocks on a
+    // lowest-priority one keep the passes at their own speed, but the rounding
+    // then waits for them: 4.52 ms).
     const bool overlap = touch && !fold && d.L > kFoldLevel && tune().overlap != 0;
     if (overlap) {
         if ((s = side_stream(di))) return s;
@@ -1218,6 +1222,7 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
         a.conv_chunks_per_image = (a.slice + kFoldChunk - 1) / kFoldChunk;
         fold_chunks = d.B * a.conv_chunks_per_image;
     }
+    cudaStream_t wst = st;   // the stream of the count, the passes and the tail rounding
     if (touch) {
         a.touch = touch_map;
         a.touch_tau = tau;
@@ -1227,10 +1232,10 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
         // the first pass reads the classes before its griddepcontrol.wait
         pl.pdl = false;
         if (!ws_zeroed && (s = launch_zero(touch_map, (int64_t)map_bytes, di->sms, st))) return s;
-        TraceScope ts(st);
+        TraceScope ts(wst);
         const int grid = (int)((d.n_param + msda::kBlockThreads - 1) / msda::kBlockThreads);
-        if (dt == MSDA_F16) msda::launch_touch_count<__half>(a, grid, st);
-        else msda::launch_touch_count<__nv_bfloat16>(a, grid, st);
+        if (dt == MSDA_F16) msda::launch_touch_count<__half>(a, grid, wst);
+        else msda::launch_touch_count<__nv_bfloat16>(a, grid, wst);
         ts.end(MSDA_KERNEL_TOUCH, d.n_param);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "touch count kernel launch");
@@ -1255,16 +1260,16 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
                 }
             }
         }
-        TraceScope ts(st);
+        TraceScope ts(wst);
         switch (dt) {
-        case MSDA_F32: msda::launch_backward<float, float>(a, lp, st); break;
+        case MSDA_F32: msda::launch_backward<float, float>(a, lp, wst); break;
         case MSDA_F16:
-            if (use_ws) msda::launch_backward<__half, float>(a, lp, st);
-            else msda::launch_backward<__half, __half>(a, lp, st);
+            if (use_ws) msda::launch_backward<__half, float>(a, lp, wst);
+            else msda::launch_backward<__half, __half>(a, lp, wst);
             break;
         default:
-            if (use_ws) msda::launch_backward<__nv_bfloat16, float>(a, lp, st);
-            else msda::launch_backward<__nv_bfloat16, __nv_bfloat16>(a, lp, st);
+            if (use_ws) msda::launch_backward<__nv_bfloat16, float>(a, lp, wst);
+            else msda::launch_backward<__nv_bfloat16, __nv_bfloat16>(a, lp, wst);
             break;
         }
         ts.end(MSDA_KERNEL_BACKWARD, d.units);
@@ -1274,11 +1279,11 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
             // fork: the rows below level 2 on the second stream
             KernelArgs ab = a;
             ab.conv_below = 1;
-            if ((e = cudaEventRecord(di->fork, st)) != cudaSuccess ||
+            if ((e = cudaEventRecord(di->fork, wst)) != cudaSuccess ||
                 (e = cudaStreamWaitEvent(di->side, di->fork, 0)) != cudaSuccess)
                 return cuda_fail(e, "fork to the second stream");
             TraceScope tb(di->side);
-            const int grid = tune().ovgrid > 0 ? di->sms * tune().ovgrid : grid_for(d.n_value / 8 / 16 + 1, di->sms);
+            const int grid = grid_for(d.n_value / 8 / 16 + 1, di->sms);
             if (dt == MSDA_F16) msda::launch_convert_tail<__half>(ab, grid, di->side);
             else msda::launch_convert_tail<__nv_bfloat16>(ab, grid, di->side);
             tb.end(MSDA_KERNEL_CONVERT, d.n_value);
@@ -1290,10 +1295,10 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     if (use_ws && (fold || touch)) {
         // the rows from the first row of level 2 on (with the folded
         // rounding), else every row, in every batch image
-        TraceScope ts(st);
+        TraceScope ts(wst);
         const int grid = grid_for(d.n_value / 8 / 16 + 1, di->sms);
-        if (dt == MSDA_F16) msda::launch_convert_tail<__half>(a, grid, st);
-        else msda::launch_convert_tail<__nv_bfloat16>(a, grid, st);
+        if (dt == MSDA_F16) msda::launch_convert_tail<__half>(a, grid, wst);
+        else msda::launch_convert_tail<__nv_bfloat16>(a, grid, wst);
         ts.end(MSDA_KERNEL_CONVERT, d.n_value);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");
