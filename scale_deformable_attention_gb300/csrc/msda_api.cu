@@ -155,7 +155,7 @@ int ilog2_floor(int v) {
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
 // params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
 // merge, nomerge, tiled, notiled, tp=<rows>, levelpass, nolevelpass, touch, notouch, tau=<n>, fold, nofold,
-// overlap, nooverlap, nol2hint.
+// overlap, nooverlap, nol2hint, c8, noc8.
 // None of them changes results beyond the rounding order of the grad_value sums.
 
 struct Tune {
@@ -175,6 +175,7 @@ struct Tune {
     int fold = -1;         // rounding folded into the level passes: -1 unless the touch classes apply, 0 off (nofold), 1 on (fold)
     int overlap = -1;      // touch classes: rounding of the finished rows on a second stream: -1 default, 0 off (nooverlap), 1 on (overlap)
     bool l2hint = true;    // TMA-gather forward: evict-first for levels over twice the L2 (off: nol2hint)
+    int c8 = -1;           // backward into the FP32 workspace, eight lanes a unit: -1 default, 0 off (noc8), 1 on (c8)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -210,6 +211,8 @@ const Tune& tune() {
             else if (!strcmp(tok, "overlap")) r.overlap = 1;
             else if (!strcmp(tok, "nooverlap")) r.overlap = 0;
             else if (!strcmp(tok, "nol2hint")) r.l2hint = false;
+            else if (!strcmp(tok, "c8")) r.c8 = 1;
+            else if (!strcmp(tok, "noc8")) r.c8 = 0;
         }
         return r;
     }();
@@ -1162,6 +1165,18 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // one corner row by different samples, instead of being fetched again.
     const int passes = level_passes(dt, d, pl, fz != nullptr, use_ws, di->l2_bytes, di->sms) ? (int)d.L : 1;
     if (passes > 1) level_pass_plan(d, pl, a);
+    // eight lanes a unit for the passes into the FP32 workspace (msda_bwd8_kernel):
+    // a corner row's load and its reduction take one L1 request each instead of
+    // two.  Measured on GB300, stress backward 4.50 -> 4.35 ms (the passes of
+    // levels 2 and 3, bound by those requests, 0.58 -> 0.53 ms alone).
+    pl.c8 = passes > 1 && use_ws && pl.spec && fz == nullptr && !pl.merge && tune().c8 != 0;
+    if (pl.c8) {
+        a.lc = 3;
+        a.lp = 0;
+        a.tpb = msda::kBlockThreads / 8;
+        pl.smem = 0;
+        pl.grid = dim3((unsigned)((d.units + a.tpb - 1) / a.tpb));
+    }
     // With one pass per level, the FP32 workspace's rows below the first row
     // of level 2 are final once passes 0 and 1 are done: the passes from
     // level 2 on (L2-bound, DRAM mostly idle) round them with extra blocks,
@@ -1192,7 +1207,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // bound by their own sampling (long-scoreboard waits on the L2), and the
     // folding blocks, which then read few workspace rows, only take their slots.
     const int tf = tune().fold;
-    const bool fold = tail_ok && d.L > kFoldLevel && (tf > 0 || (tf < 0 && !touch));
+    // (msda_bwd8_kernel has no folding blocks)
+    const bool fold = tail_ok && d.L > kFoldLevel && !pl.c8 && (tf > 0 || (tf < 0 && !touch));
     // With the touch classes, the rows below level 2's first row are final once
     // passes 0 and 1 are done: a second stream rounds them while the passes
     // from level 2 on run (those are bound by the L2, the rounding by DRAM), and

@@ -1598,6 +1598,220 @@ __global__ void __launch_bounds__(kBlockThreads, 4) msda_bwd4_merge1_kernel(cons
 }
 
 // ---------------------------------------------------------------------------
+// Backward into the FP32 workspace for 16-bit I/O, eight channel lanes a unit
+// (one pass per level, no corner merge).  Lane c owns channels [4c, 4c + 4)
+// of each 32-channel group: its corner loads are 8 bytes and its reductions
+// 16 bytes of fp32, so the eight lanes of a team read a corner row's 64 bytes
+// with one request and add its 128 bytes of sums with one, where the four
+// lanes of msda_bwd4_kernel take two of each (split slots).  The passes of
+// dense levels, whose corner rows mostly hit in the L2, are bound by the
+// L1's requests to the L2.  Setup, gather, touch classes and scatter as in
+// bwd4_body: lane c sets up sample r0 + c of the round, the team reads it
+// with warp shuffles.
+
+// four 16-bit channels (8 bytes) -> fp32
+__device__ __forceinline__ void unpack8(const uint2& w, float (&f)[4], const __nv_bfloat16*) {
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xffff0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xffff0000u);
+}
+__device__ __forceinline__ void unpack8(const uint2& w, float (&f)[4], const __half*) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&w.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&w.y));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+}
+
+constexpr int kC8 = 8;
+
+template <typename T, int NV, bool TOUCH>
+__global__ void __launch_bounds__(kBlockThreads) msda_bwd8_kernel(const KernelArgs a) {
+    static_assert(sizeof(T) == 2, "16-bit I/O into the fp32 workspace");
+    constexpr int JB = 2;   // samples whose corners are loaded together
+    const T* tag = nullptr;
+    __shared__ Level lv[MSDA_MAX_LEVELS];
+    if (threadIdx.x < a.L) {
+        lv[threadIdx.x] = level_of(a, threadIdx.x);
+        if (!lv[threadIdx.x].ok) atomicOr(a.err, kErrBadLevel);
+    }
+    __syncthreads();
+    // launched as a programmatic dependent of the workspace's clearing: wait
+    // for it before anything (returns at once otherwise)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int team = threadIdx.x / kC8, c = threadIdx.x % kC8;
+    const int lane0 = (threadIdx.x & 31) & ~(kC8 - 1);
+    const uint32_t u = blockIdx.x * (uint32_t)(kBlockThreads / kC8) + (uint32_t)team;
+    const bool active = u < (uint32_t)a.n_units;
+    const uint32_t b = active ? fdiv(u, a.div_qm) : 0u;
+    const uint32_t m = active ? u - fdiv(u, a.div_m) * (uint32_t)a.M : 0u;
+    const int MD = a.M * a.D;
+    const long long vofs = (long long)b * a.slice + (long long)m * a.D + 4 * c;
+    const T* vbase = reinterpret_cast<const T*>(a.value) + vofs;
+    float* gbase = reinterpret_cast<float*>(a.grad_acc) + vofs;
+    T* tbase = TOUCH ? reinterpret_cast<T*>(a.touch_out) + vofs : nullptr;
+    float g[NV][4];
+#pragma unroll
+    for (int n = 0; n < NV; ++n) {
+        if (active) {
+            const T* go = reinterpret_cast<const T*>(a.grad_out) + (long long)u * a.D + 32 * n + 4 * c;
+            unpack8(__ldg(reinterpret_cast<const uint2*>(go)), g[n], tag);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) g[n][e] = 0.f;
+        }
+    }
+    T* gl = reinterpret_cast<T*>(a.grad_loc);
+    T* ga = reinterpret_cast<T*>(a.grad_attn);
+
+    for (int r0 = a.s_begin; r0 < a.s_end; r0 += kC8) {
+        const int nj = min(kC8, a.s_end - r0);   // samples of this round (the same for the whole warp)
+        const int s_own = r0 + c;
+        const bool live = active && c < nj;
+        float x = -4.f, y = -4.f, wa = 0.f;
+        int l = 0;
+        if (live) {
+            const long long ps = (long long)u * a.LK + s_own;
+            const T* pl = reinterpret_cast<const T*>(a.loc) + 2 * ps;
+            x = ldg_f(pl);
+            y = ldg_f(pl + 1);
+            wa = ldg_f(reinterpret_cast<const T*>(a.attn) + ps);
+            l = (int)fdiv((uint32_t)s_own, a.div_k);
+        }
+        Level lev = lv[l];
+        if (!live) lev.ok = 0;
+        const SampleSetup me = sample_setup(lev, x, y, MD);
+        unsigned tw[4] = {0u, 0u, 0u, 0u};
+        bool tsp = false;
+        if constexpr (TOUCH) {
+            tsp = live && touch_sparse(a, lev);
+            if (tsp) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if ((me.mask >> k) & 1u)
+                        tw[k] = __ldg(a.touch + (touch_row(a, b, me.pix + (k & 1) + (k >> 1) * lev.W, m) >> 4));
+            }
+        }
+
+        // gather + reduce over the team: lane j keeps the totals of sample j
+        float ra = 0.f, rx = 0.f, ry = 0.f;
+        for (int j0 = 0; j0 < nj; j0 += JB) {
+            uint2 raw[JB][4][NV];
+            SampleSetup st[JB];
+#pragma unroll
+            for (int jj = 0; jj < JB; ++jj) {
+                st[jj] = shfl_setup(me, lane0 + min(j0 + jj, kC8 - 1));
+                if (j0 + jj >= nj) st[jj].mask = 0u;
+                const int off[4] = {st[jj].o, st[jj].o + MD, st[jj].o + st[jj].wmd, st[jj].o + st[jj].wmd + MD};
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+#pragma unroll
+                    for (int n = 0; n < NV; ++n)
+                        raw[jj][k][n] = ((st[jj].mask >> k) & 1u)
+                                            ? __ldg(reinterpret_cast<const uint2*>(vbase + off[k] + 32 * n))
+                                            : make_uint2(0u, 0u);
+            }
+#pragma unroll
+            for (int jj = 0; jj < JB; ++jj) {
+                float d[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float t = 0.f;
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) {
+                        float v[4];
+                        unpack8(raw[jj][k][n], v, tag);
+                        t = __fmaf_rn(g[n][0], v[0], t);
+                        t = __fmaf_rn(g[n][1], v[1], t);
+                        t = __fmaf_rn(g[n][2], v[2], t);
+                        t = __fmaf_rn(g[n][3], v[3], t);
+                    }
+                    d[k] = t;
+                }
+                float w[4];
+                corner_weights(st[jj].lx, st[jj].ly, w);
+                const bool any = st[jj].mask != 0u;
+                const float lx = st[jj].lx, ly = st[jj].ly;
+                float pa = any ? (w[0] * d[0] + w[1] * d[1] + w[2] * d[2] + w[3] * d[3]) : 0.f;
+                float px = any ? ((1.f - ly) * (d[1] - d[0]) + ly * (d[3] - d[2])) : 0.f;
+                float py = any ? ((1.f - lx) * (d[2] - d[0]) + lx * (d[3] - d[1])) : 0.f;
+#pragma unroll
+                for (int o = 1; o < kC8; o <<= 1) {
+                    pa += __shfl_xor_sync(0xffffffffu, pa, o);
+                    px += __shfl_xor_sync(0xffffffffu, px, o);
+                    py += __shfl_xor_sync(0xffffffffu, py, o);
+                }
+                if (c == j0 + jj) {
+                    ra = pa;
+                    rx = px;
+                    ry = py;
+                }
+            }
+        }
+        if (live) {
+            const long long ps = (long long)u * a.LK + s_own;
+            ga[ps] = Elem<T>::from_f(ra);
+            gl[2 * ps] = Elem<T>::from_f(wa * lev.fW * rx);
+            gl[2 * ps + 1] = Elem<T>::from_f(wa * lev.fH * ry);
+        }
+
+        // the sample's corner classes, 2 bits each (2 = reduce into the workspace)
+        unsigned tcls = 0xAAu;
+        if constexpr (TOUCH) {
+            if (tsp) {
+                tcls = 0u;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    unsigned cl = 2u;
+                    if ((me.mask >> k) & 1u) {
+                        cl = touch_bits(tw[k], touch_row(a, b, me.pix + (k & 1) + (k >> 1) * lev.W, m));
+                        if (cl == 0u) {   // the count pass missed it: never expected
+                            atomicOr(a.err, kErrTouch);
+                            cl = 2u;
+                        }
+                    }
+                    tcls |= cl << (2 * k);
+                }
+            }
+        }
+        float w0[4];
+        corner_weights(me.lx, me.ly, w0);
+        float mc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mc[k] = wa * w0[k];
+
+        // scatter: A * w_corner * g into the inside corners
+        for (int j = 0; j < nj; ++j) {
+            const int src = lane0 + j;
+            const int so = __shfl_sync(0xffffffffu, me.o, src);
+            const int swmd = __shfl_sync(0xffffffffu, me.wmd, src);
+            const unsigned smk = __shfl_sync(0xffffffffu, me.mask, src);
+            const unsigned scls = TOUCH ? __shfl_sync(0xffffffffu, tcls, src) : 0xAAu;
+            float cj[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cj[k] = __shfl_sync(0xffffffffu, mc[k], src);
+            const int off[4] = {so, so + MD, so + swmd, so + swmd + MD};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (!((smk >> k) & 1u)) continue;
+                const float2 cf = make_float2(cj[k], cj[k]);
+#pragma unroll
+                for (int n = 0; n < NV; ++n) {
+                    const float2 t0 = __fmul2_rn(cf, make_float2(g[n][0], g[n][1]));
+                    const float2 t1 = __fmul2_rn(cf, make_float2(g[n][2], g[n][3]));
+                    if (TOUCH && ((scls >> (2 * k)) & 3u) == 1u)
+                        store4<T>(tbase + off[k] + 32 * n, t0.x, t0.y, t1.x, t1.y);   // the row's one contribution
+                    else
+                        red_v4_f32(gbase + off[k] + 32 * n, t0.x, t0.y, t1.x, t1.y);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Forward with TMA gathers (rows of whole 16-byte vectors, L*K in {4, 8, 16,
 // 32}, B*S*M < 2^31).  `value` is seen as a 2-D tensor of B*S*M rows of D
 // channels; one cp.async.bulk.tensor ... tile::gather4 brings the four

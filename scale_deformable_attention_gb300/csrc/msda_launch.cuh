@@ -22,6 +22,7 @@ struct Plan {
     bool pdl;      // launched as a programmatic dependent of the kernel ahead of it
     bool fused;    // fused operator (offsets + logits in, offset / logit gradients out)
     bool merge;    // backward: merge the corners a point group's samples share before the scatter
+    bool c8;       // backward into the fp32 workspace, 16-bit I/O: eight lanes a unit (msda_bwd8_kernel)
 };
 
 #define MSDA_DISPATCH_NV(NVV, ...)                                   \
@@ -88,6 +89,11 @@ static void bwd4_go2(const KernelArgs& a, const Plan& pl, cudaStream_t st) {
     // each accumulator)
     constexpr int MODE = (std::is_same<ACC, float>::value && sizeof(T) == 2) ? kMergeCorners : kMergeCells;
     if constexpr (std::is_same<ACC, float>::value && sizeof(T) == 2 && !FUSED) {
+        if (pl.c8) {
+            if (a.touch) launch_plan(msda_bwd8_kernel<T, NV, true>, a, pl, st);
+            else launch_plan(msda_bwd8_kernel<T, NV, false>, a, pl, st);
+            return;
+        }
         // the touch classes of the workspace rows: their own kernel (its
         // extra registers stay out of the others), without the corner merge
         if (a.touch) {

@@ -6,7 +6,8 @@ corner merge forced on and off, ordinary (non-programmatic) launches, and
 the FP32 accumulator on chip forced on (with tiles of 16 rows: most points
 straddle tiles) and off, and the backward run one pass per level (with and
 without the corner merge, with the touch classes of the FP32 workspace's
-rows off, and with every level or no level sparse) or in one pass.  Each runs in a
+rows off, with every level or no level sparse, with four lanes a unit
+instead of eight) or in one pass.  Each runs in a
 child process with MSDA_TUNE set."""
 import os
 import subprocess
@@ -21,7 +22,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 @pytest.mark.parametrize("tune", ["tma", "generic", "params=direct", "params=ld", "notma,P=1", "P=8", "pointparallel",
                                   "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled",
                                   "levelpass", "levelpass,merge", "nolevelpass", "levelpass,nomerge",
-                                  "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000", "levelpass,overlap"])
+                                  "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000", "levelpass,overlap",
+                                  "levelpass,noc8", "levelpass,noc8,notouch"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
