@@ -1183,7 +1183,7 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // and the rounding pass afterwards handles the remaining rows only.
     constexpr int kFoldLevel = 2;
     constexpr long long kFoldChunk = 1 << 16;   // workspace elements per folding block
-    // rounding by the tail kernel (msda_convert_tail_kernel): one pass per level,
+    // rounding by the tail kernel (msda_round_rows_kernel): one pass per level,
     // 16-byte aligned grad_value, whole 8-element groups
     const bool tail_ok = passes > 1 && use_ws && pl.spec && fz == nullptr && aligned(grad_value, 16) &&
                          (d.S * d.M * d.D) % 8 == 0;
@@ -1300,8 +1300,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
                 return cuda_fail(e, "fork to the second stream");
             TraceScope tb(di->side);
             const int grid = grid_for(d.n_value / 8 / 16 + 1, di->sms);
-            if (dt == MSDA_F16) msda::launch_convert_tail<__half>(ab, grid, di->side);
-            else msda::launch_convert_tail<__nv_bfloat16>(ab, grid, di->side);
+            if (dt == MSDA_F16) msda::launch_round_rows<__half>(ab, pl.nv, grid, di->side);
+            else msda::launch_round_rows<__nv_bfloat16>(ab, pl.nv, grid, di->side);
             tb.end(MSDA_KERNEL_CONVERT, d.n_value);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "convert kernel launch");
             if ((e = cudaEventRecord(di->join, di->side)) != cudaSuccess)
@@ -1313,8 +1313,8 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
         // rounding), else every row, in every batch image
         TraceScope ts(wst);
         const int grid = grid_for(d.n_value / 8 / 16 + 1, di->sms);
-        if (dt == MSDA_F16) msda::launch_convert_tail<__half>(a, grid, wst);
-        else msda::launch_convert_tail<__nv_bfloat16>(a, grid, wst);
+        if (dt == MSDA_F16) msda::launch_round_rows<__half>(a, pl.nv, grid, wst);
+        else msda::launch_round_rows<__nv_bfloat16>(a, pl.nv, grid, wst);
         ts.end(MSDA_KERNEL_CONVERT, d.n_value);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "convert kernel launch");

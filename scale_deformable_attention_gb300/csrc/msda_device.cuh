@@ -1943,9 +1943,10 @@ __global__ void __launch_bounds__(kTmaWarps * 32) msda_fwd_tma_kernel(const Kern
     __syncwarp();
     // L2 priority by the size of the sample's level (its rows in one image):
     // the rows of a level over twice the L2 are read about once each and evict
-    // first.  Measured on GB300 (stress forward): 0.843 -> 0.825 ms; evict-last
-    // for the levels of at most a quarter of the L2 gave nothing (0.839 ms), at
-    // a fraction of 0.25 0.872 ms, and with both priorities 1.10 ms.
+    // first.  Measured on GB300 (stress forward): 0.843 -> 0.825 ms; evict-first
+    // from half the L2 on (levels 0 and 1) 0.859 ms, from an eighth 1.07 ms;
+    // evict-last for the levels of at most a quarter of the L2 gave nothing
+    // (0.839 ms), at a fraction of 0.25 0.872 ms, and with both priorities 1.10 ms.
     const long long lvb = (long long)lev.fH * lev.W * a.M * a.D * (long long)sizeof(T);
     const bool evict_first = a.l2_bytes > 0 && lvb >= 2 * a.l2_bytes;
     if (live) {
@@ -2191,79 +2192,77 @@ __global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, 
 // The rounding pass for the rows the backward passes did not round
 // themselves: in every batch image, the rows from the first row of the levels
 // >= a.conv_level on (below it with a.conv_below), every row with
-// a.conv_level < 0 (16-byte aligned workspace and grad_value, slices of a
-// multiple of 8 elements).
-template <typename T>
-__global__ void __launch_bounds__(kBlockThreads, 8) msda_convert_tail_kernel(const KernelArgs a) {
-    static_assert(sizeof(T) == 2, "eight 16-bit elements are one 16-byte store");
+// a.conv_level < 0 (16-byte aligned workspace and grad_value; rows of 32*NV
+// channels, the specialised plans).  A warp takes 32 consecutive rows (pixel,
+// head) of one image; lane L works out the class of row base + L once (touch
+// classes: 0 untouched, 1 written by its pass, 2 in the workspace), then the
+// warp rounds the rows four at a time, eight lanes a row and 16 bytes of fp32
+// a lane (each 32-channel group of a row is one 128-byte line), reading a
+// row's class from its lane with a shuffle.  Loads of four rows are issued
+// before their stores; the rows read are re-zeroed without looking (with
+// MSDA_BWD_WORKSPACE_ZEROED).  Measured on GB300 (stress rounding, 8.6 GB of
+// workspace): 1.36 ms, against 1.41 ms for one thread per group of eight
+// elements (two groups in flight, eight blocks an SM; four groups 1.53 ms,
+// eight 1.92 ms; with a test of the values before re-zeroing 1.49 ms).
+template <typename T, int NV>
+__global__ void __launch_bounds__(kBlockThreads) msda_round_rows_kernel(const KernelArgs a) {
+    static_assert(sizeof(T) == 2, "16-bit grad_value");
+    const T* tag = nullptr;
     __shared__ long long cut;
     __shared__ TouchRanges tr;
-    if (threadIdx.x == 0) cut = a.conv_level < 0 ? 0 : first_row_from(a, a.conv_level) * a.M * a.D;
+    if (threadIdx.x == 0) cut = a.conv_level < 0 ? 0 : first_row_from(a, a.conv_level) * a.M;
     if (a.touch) touch_ranges(a, &tr);
     else __syncthreads();
-    const long long g0 = a.conv_below ? 0 : cut / 8, n8 = a.conv_below ? cut / 8 : a.slice / 8;
-    // U groups of eight elements a thread in flight: their touch words are
-    // loaded together, then the workspace rows they need, then the stores.
-    // Measured on GB300 (stress rounding, 8.6 GB of workspace): U = 2 at
-    // eight blocks an SM 1.47 ms; U = 4 (57 registers, four blocks) 1.53 ms,
-    // U = 2 at four blocks 1.75 ms, U = 8 1.92 ms.
-    constexpr int U = 2;
-    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long nth = (long long)gridDim.x * blockDim.x;
+    const long long rows = a.S * a.M;
+    const long long r_lo = a.conv_below ? 0 : cut, r_hi = a.conv_below ? cut : rows;
+    const int lane = threadIdx.x & 31, j = lane & 7, sub = lane >> 3;
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    constexpr int D = 32 * NV;
     for (int img = 0; img < a.n_images; ++img) {
-        const float4* ws = reinterpret_cast<const float4*>(reinterpret_cast<float*>(a.grad_acc) + img * a.slice);
-        float4* wz = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.grad_acc) + img * a.slice);
+        const float* ws = reinterpret_cast<const float*>(a.grad_acc) + img * a.slice;
+        float* wz = reinterpret_cast<float*>(a.grad_acc) + img * a.slice;
         T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
-        for (long long i0 = g0 + tid; i0 < n8; i0 += U * nth) {
-            // class of each group's row: 0 untouched, 1 written by the sampling
-            // pass, 2 reduced into the workspace (every row of a dense level)
-            unsigned cls[U], id[U];
+        for (long long base = r_lo + warp * 32; base < r_hi; base += nwarps * 32) {
+            // class of row base + lane: 0 untouched (sparse level), 1 written by its
+            // pass, 2 in the workspace (every row of a dense level); 1 past the range
+            const long long r = base + lane;
+            unsigned cls = r < r_hi ? 2u : 1u;
+            if (a.touch && r < r_hi) {
+                const unsigned row = (unsigned)r;
+                bool sp = false;
+                for (int q = 0; q < tr.n; ++q) sp |= row >= tr.begin[q] && row < tr.end[q];
+                if (sp) {
+                    const unsigned pix = fdiv(row, a.div_m);
+                    const unsigned id = ((unsigned)img * (unsigned)a.M + (row - pix * (unsigned)a.M)) * (unsigned)a.S + pix;
+                    cls = min(touch_bits(__ldg(a.touch + (id >> 4)), id), 2u);
+                }
+            }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const long long i = i0 + u * nth;
-                cls[u] = i < n8 ? 2u : 4u;   // 4: past the end
-                id[u] = 0u;
-                if (a.touch && i < n8) {
-                    const unsigned row = fdiv((uint32_t)i, a.div_d8);
-                    bool sp = false;
-                    for (int j = 0; j < tr.n; ++j) sp |= row >= tr.begin[j] && row < tr.end[j];
-                    if (sp) {
-                        const unsigned pix = fdiv(row, a.div_m);
-                        id[u] = ((unsigned)img * (unsigned)a.M + (row - pix * (unsigned)a.M)) * (unsigned)a.S + pix;
-                        cls[u] = 3u;   // sparse: from its touch word below
+            for (int q0 = 0; q0 < 8; q0 += 4) {
+                unsigned c4[4];
+                float4 x[4][NV];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int rl = 4 * (q0 + q) + sub;   // the row's lane
+                    c4[q] = __shfl_sync(0xffffffffu, cls, rl);
+                    const long long e = (base + rl) * D + 4 * j;
+#pragma unroll
+                    for (int n = 0; n < NV; ++n)
+                        x[q][n] = c4[q] == 2u ? __ldcs(reinterpret_cast<const float4*>(ws + e + 32 * n))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (c4[q] == 1u) continue;
+                    const long long e = (base + 4 * (q0 + q) + sub) * D + 4 * j;
+#pragma unroll
+                    for (int n = 0; n < NV; ++n) {
+                        *reinterpret_cast<uint2*>(gv + e + 32 * n) =
+                            make_uint2(pack2(x[q][n].x, x[q][n].y, tag), pack2(x[q][n].z, x[q][n].w, tag));
+                        if (c4[q] == 2u && a.conv_rezero)
+                            __stcs(reinterpret_cast<float4*>(wz + e + 32 * n), make_float4(0.f, 0.f, 0.f, 0.f));
                     }
-                }
-            }
-            unsigned w[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) w[u] = cls[u] == 3u ? __ldg(a.touch + (id[u] >> 4)) : 0u;
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (cls[u] == 3u) cls[u] = min(touch_bits(w[u], id[u]), 2u);
-            float4 x[U], y[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const long long i = i0 + u * nth;
-                if (cls[u] == 2u) {
-                    x[u] = __ldcs(ws + 2 * i);
-                    y[u] = __ldcs(ws + 2 * i + 1);
-                } else {
-                    x[u] = y[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const long long i = i0 + u * nth;
-                if (cls[u] == 0u || cls[u] == 2u) {
-                    const float f[8] = {x[u].x, x[u].y, x[u].z, x[u].w, y[u].x, y[u].y, y[u].z, y[u].w};
-                    Slot<T, 8>::store(gv + 8 * i, f);
-                }
-                // re-zeroed without looking: rows read here have taken contributions
-                // (dense levels: almost all; sparse levels: class 2), and skipping
-                // the test on the values was faster (stress rounding 1.49 -> 1.43 ms)
-                if (cls[u] == 2u && a.conv_rezero) {
-                    __stcs(wz + 2 * i, make_float4(0.f, 0.f, 0.f, 0.f));
-                    __stcs(wz + 2 * i + 1, make_float4(0.f, 0.f, 0.f, 0.f));
                 }
             }
         }

@@ -6,7 +6,7 @@
 namespace msda {
 template void launch_backward<__half, float>(const KernelArgs&, const Plan&, cudaStream_t);
 template void launch_convert<__half>(float*, __half*, long long, int, int, int, cudaStream_t);
-template void launch_convert_tail<__half>(const KernelArgs&, int, cudaStream_t);
 template void launch_touch_count<__half>(const KernelArgs&, int, cudaStream_t);
+template void launch_round_rows<__half>(const KernelArgs&, int, int, cudaStream_t);
 template void launch_widen<__half>(const __half*, float*, long long, int, cudaStream_t);
 }  // namespace msda

@@ -194,8 +194,8 @@ void launch_convert(float* ws, T* gv, long long n, int vec, int rezero, int grid
 }
 
 template <typename T>
-void launch_convert_tail(const KernelArgs& a, int grid, cudaStream_t st) {
-    msda_convert_tail_kernel<T><<<grid, kBlockThreads, 0, st>>>(a);
+void launch_round_rows(const KernelArgs& a, int nv, int grid, cudaStream_t st) {
+    MSDA_DISPATCH_NV(nv, (msda_round_rows_kernel<T, NV><<<grid, kBlockThreads, 0, st>>>(a)));
 }
 
 template <typename T>
@@ -273,8 +273,8 @@ MSDA_EXTERN_IO(__nv_bfloat16)
     extern template void launch_backward<T, T>(const KernelArgs&, const Plan&, cudaStream_t);           \
     extern template void launch_convert<T>(float*, T*, long long, int, int, int, cudaStream_t);         \
     extern template void launch_widen<T>(const T*, float*, long long, int, cudaStream_t);                \
-    extern template void launch_convert_tail<T>(const KernelArgs&, int, cudaStream_t);            \
-    extern template void launch_touch_count<T>(const KernelArgs&, int, cudaStream_t);
+    extern template void launch_touch_count<T>(const KernelArgs&, int, cudaStream_t);                \
+    extern template void launch_round_rows<T>(const KernelArgs&, int, int, cudaStream_t);
 MSDA_EXTERN_HALF(__half)
 MSDA_EXTERN_HALF(__nv_bfloat16)
 #undef MSDA_EXTERN_HALF
