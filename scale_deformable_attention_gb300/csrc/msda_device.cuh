@@ -110,7 +110,8 @@ struct KernelArgs {
     // below the first row of levels >= conv_level, which no pass from
     // conv_level on adds to.  conv_first: this launch's first chunk.
     int conv_blocks, conv_every, conv_level, conv_rezero;
-    int conv_below;        // tail rounding: the rows below that first row instead of from it on
+    int conv_lo, conv_hi;  // tail rounding: rows from the first row of the levels >= conv_lo (row 0 when < 0)
+                           // up to the first row of the levels >= conv_hi (the end when >= L)
     long long conv_first, conv_chunk, conv_chunks_per_image;
     void* conv_out;
     int n_images;          // B
@@ -2191,9 +2192,9 @@ __global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, 
 
 // The rounding pass for the rows the backward passes did not round
 // themselves: in every batch image, the rows from the first row of the levels
-// >= a.conv_level on (below it with a.conv_below), every row with
-// a.conv_level < 0 (16-byte aligned workspace and grad_value; rows of 32*NV
-// channels, the specialised plans).  A warp takes 32 consecutive rows (pixel,
+// >= a.conv_lo (row 0 when a.conv_lo < 0) up to the first row of the levels
+// >= a.conv_hi, which no pass of those levels adds to (16-byte aligned
+// workspace and grad_value; rows of 32*NV channels, the specialised plans).  A warp takes 32 consecutive rows (pixel,
 // head) of one image; lane L works out the class of row base + L once (touch
 // classes: 0 untouched, 1 written by its pass, 2 in the workspace), then the
 // warp rounds the rows four at a time, eight lanes a row and 16 bytes of fp32
@@ -2208,13 +2209,15 @@ template <typename T, int NV>
 __global__ void __launch_bounds__(kBlockThreads) msda_round_rows_kernel(const KernelArgs a) {
     static_assert(sizeof(T) == 2, "16-bit grad_value");
     const T* tag = nullptr;
-    __shared__ long long cut;
+    __shared__ long long lo_hi[2];
     __shared__ TouchRanges tr;
-    if (threadIdx.x == 0) cut = a.conv_level < 0 ? 0 : first_row_from(a, a.conv_level) * a.M;
+    if (threadIdx.x == 0) {
+        lo_hi[0] = a.conv_lo < 0 ? 0 : first_row_from(a, a.conv_lo) * a.M;
+        lo_hi[1] = first_row_from(a, a.conv_hi) * a.M;   // S * M for conv_hi >= L
+    }
     if (a.touch) touch_ranges(a, &tr);
     else __syncthreads();
-    const long long rows = a.S * a.M;
-    const long long r_lo = a.conv_below ? 0 : cut, r_hi = a.conv_below ? cut : rows;
+    const long long r_lo = lo_hi[0], r_hi = lo_hi[1];
     const int lane = threadIdx.x & 31, j = lane & 7, sub = lane >> 3;
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
