@@ -1212,7 +1212,9 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // With the touch classes, the rows below level 2's first row are final once
     // passes 0 and 1 are done: a second stream rounds them while the passes
     // from level 2 on run (those are bound by the L2, the rounding by DRAM), and
-    // the tail kernel afterwards rounds the rest.  Measured on GB300, stress
+    // the tail kernel afterwards rounds the rest.  (The count of levels 1 to 3
+    // on that stream beside pass 0 gained nothing: pass 0 slowed by what the
+    // count saved.)  Measured on GB300, stress
     // backward: 4.67 -> 4.50 ms (the second stream's rounding at the tail
     // kernel's grid; at one, two or four blocks an SM it takes 7.0, 4.1 and
     // 3.1 ms and the backward 8.9, 6.2 and 5.2 ms; the passes on a
