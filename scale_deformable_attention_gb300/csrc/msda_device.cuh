@@ -1631,7 +1631,7 @@ constexpr int kC8 = 8;
 template <typename T, int NV, bool TOUCH>
 __global__ void __launch_bounds__(kBlockThreads) msda_bwd8_kernel(const KernelArgs a) {
     static_assert(sizeof(T) == 2, "16-bit I/O into the fp32 workspace");
-    constexpr int JB = 2;   // samples whose corners are loaded together
+    constexpr int JB = 2;   // samples whose corners are loaded together (stress backward 4.12 ms; 4 or 1: 4.26)
     const T* tag = nullptr;
     __shared__ Level lv[MSDA_MAX_LEVELS];
     if (threadIdx.x < a.L) {
