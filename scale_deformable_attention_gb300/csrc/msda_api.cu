@@ -48,6 +48,7 @@ bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) %
 
 struct DeviceInfo {
     bool init = false;
+    unsigned long long ctx = 0;   // id of the context the fields below belong to (0: unknown)
     int sms = 0;
     int l2_bytes = 0;
     unsigned* err = nullptr;  // device address of g_msda_err on this device
@@ -63,18 +64,57 @@ std::mutex g_dev_mu;
 }  // namespace
 
 // Device error word (see msda_device_errors).  One copy per device; its device
-// address is looked up once per device with cudaGetSymbolAddress.
+// address is looked up once per device context with cudaGetSymbolAddress.
 __device__ unsigned int g_msda_err;
 
 namespace {
+
+// Id of the calling thread's current context (cuCtxGetId: never reused in a
+// process), or 0 when the driver does not give one.
+unsigned long long current_context_id() {
+    using GetCurrent = PFN_cuCtxGetCurrent_v4000;
+    using GetId = PFN_cuCtxGetId_v12000;
+    static GetCurrent get_current = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? (GetCurrent)p
+                   : (GetCurrent) nullptr;
+    }();
+    static GetId get_id = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        return cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+                       q == cudaDriverEntryPointSuccess
+                   ? (GetId)p
+                   : (GetId) nullptr;
+    }();
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&c) == CUDA_SUCCESS && c && get_id(c, &id) == CUDA_SUCCESS) return id;
+    return 0;
+}
 
 msda_status device_info(DeviceInfo** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(MSDA_ERR_CUDA, "device ordinal %d out of range", dev);
+    // a device reset (cudaDeviceReset) gives the device a new context: the
+    // error word's address, the second stream and its events of the old one
+    // are then stale and are looked up or created again (the old handles are
+    // gone with their context and are not released)
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_dev_mu);
     DeviceInfo& d = g_dev[dev];
+    if (d.init && ctx != 0 && ctx != d.ctx) {
+        std::lock_guard<std::mutex> sl(d.side_mu);
+        d.init = false;
+        d.err = nullptr;
+        d.side = nullptr;
+        d.fork = d.join = nullptr;
+    }
     if (!d.init) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
@@ -84,6 +124,7 @@ msda_status device_info(DeviceInfo** out) {
         e = cudaGetSymbolAddress(&p, g_msda_err);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
         d.err = static_cast<unsigned*>(p);
+        d.ctx = ctx;
         d.init = true;
     }
     *out = &d;
