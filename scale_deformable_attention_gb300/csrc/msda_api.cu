@@ -1206,18 +1206,6 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
     // one corner row by different samples, instead of being fetched again.
     const int passes = level_passes(dt, d, pl, fz != nullptr, use_ws, di->l2_bytes, di->sms) ? (int)d.L : 1;
     if (passes > 1) level_pass_plan(d, pl, a);
-    // eight lanes a unit for the passes into the FP32 workspace (msda_bwd8_kernel):
-    // a corner row's load and its reduction take one L1 request each instead of
-    // two.  Measured on GB300, stress backward 4.50 -> 4.35 ms (the passes of
-    // levels 2 and 3, bound by those requests, 0.58 -> 0.53 ms alone).
-    pl.c8 = passes > 1 && use_ws && pl.spec && fz == nullptr && !pl.merge && tune().c8 != 0;
-    if (pl.c8) {
-        a.lc = 3;
-        a.lp = 0;
-        a.tpb = msda::kBlockThreads / 8;
-        pl.smem = 0;
-        pl.grid = dim3((unsigned)((d.units + a.tpb - 1) / a.tpb));
-    }
     // With one pass per level, the FP32 workspace's rows below the first row
     // of level 2 are final once passes 0 and 1 are done: the passes from
     // level 2 on (L2-bound, DRAM mostly idle) round them with extra blocks,
@@ -1241,22 +1229,38 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
                        workspace_bytes >= map_off + map_bytes;
     unsigned* touch_map = touch ? reinterpret_cast<unsigned*>(static_cast<unsigned char*>(workspace) + map_off)
                                 : nullptr;
+    // Eight lanes a unit for the passes into the FP32 workspace (msda_bwd8_kernel):
+    // a corner row's load and its reduction take one L1 request each instead of
+    // two.  Measured on GB300, stress backward with the touch classes 4.50 ->
+    // 4.35 ms (the passes of levels 2 and 3, bound by those requests, 0.58 ->
+    // 0.53 ms alone).  It has no folding blocks, and without the touch classes
+    // the four-lane passes with the folded rounding are faster (5.60 against
+    // 5.69 ms), so by default it runs with the classes only (c8 forces it).
+    pl.c8 = passes > 1 && use_ws && pl.spec && fz == nullptr && !pl.merge &&
+            (tune().c8 > 0 || (tune().c8 < 0 && touch));
+    if (pl.c8) {
+        a.lc = 3;
+        a.lp = 0;
+        a.tpb = msda::kBlockThreads / 8;
+        pl.smem = 0;
+        pl.grid = dim3((unsigned)((d.units + a.tpb - 1) / a.tpb));
+    }
     // With the rounding folded into the passes from level 2 on, the rows below
     // level 2's first row, final once passes 0 and 1 are done, are rounded by
     // extra blocks of those passes, and the tail kernel rounds the rest.  Not
     // with the touch classes by default: the passes of the coarse levels are
     // bound by their own sampling (long-scoreboard waits on the L2), and the
-    // folding blocks, which then read few workspace rows, only take their slots.
+    // folding blocks, which then read few workspace rows, only take their slots
+    // (and msda_bwd8_kernel has no folding blocks).
     const int tf = tune().fold;
-    // (msda_bwd8_kernel has no folding blocks)
     const bool fold = tail_ok && d.L > kFoldLevel && !pl.c8 && (tf > 0 || (tf < 0 && !touch));
     // With the touch classes, the rows below level 2's first row are final once
     // passes 0 and 1 are done: a second stream rounds them while the passes
     // from level 2 on run (those are bound by the L2, the rounding by DRAM), and
     // the tail kernel afterwards rounds the rest.  (The count of levels 1 to 3
     // on that stream beside pass 0 gained nothing: pass 0 slowed by what the
-    // count saved.)  Measured on GB300, stress
-    // backward: 4.67 -> 4.50 ms (the second stream's rounding at the tail
+    // count saved.)  Measured on GB300, stress backward: 4.67 -> 4.50 ms (the
+    // second stream's rounding at the tail
     // kernel's grid; at one, two or four blocks an SM it takes 7.0, 4.1 and
     // 3.1 ms and the backward 8.9, 6.2 and 5.2 ms; the passes on a
     // highest-priority stream and the rounding in short blocks on a

@@ -23,7 +23,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
                                   "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled",
                                   "levelpass", "levelpass,merge", "nolevelpass", "levelpass,nomerge",
                                   "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000", "levelpass,overlap",
-                                  "levelpass,noc8", "levelpass,noc8,notouch"])
+                                  "levelpass,noc8", "levelpass,c8,notouch"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():

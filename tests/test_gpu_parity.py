@@ -437,6 +437,32 @@ def test_workspace_zeroed_flag(dtype, accumulate):
         assert int(torch.count_nonzero(ws)) == 0, "the workspace must hold zeros after the call"
 
 
+@pytest.mark.parametrize("zeroed", [False, True])
+def test_level_passes_accumulate(zeroed):
+    """MSDA_BWD_ACCUMULATE on a problem with one backward pass per level: the
+    workspace starts from the widened grad_value (no touch classes then: every
+    row goes through the workspace), the passes add to it, the rounding adds
+    nothing more.  Against the oracle plus the starting values."""
+    msda = _msda()
+    shapes = ((256, 256), (128, 128), (64, 64), (32, 32))
+    wl = W.WORKLOADS["decoder_bf16"].with_(B=2, Q=15000, shapes=shapes, seed=52)
+    inp = W.make_inputs(wl)
+    t = to_torch(inp, "bf16", DEV)
+    dims = (wl.B, wl.S, wl.M, wl.D, wl.L, wl.K, wl.Qn)
+    ws = torch.zeros(msda.workspace_size(torch.bfloat16, "fp32", dims) // 4, dtype=torch.float32, device=DEV)
+    start = torch.randn(t["value"].shape, generator=torch.Generator().manual_seed(52)).to(DEV).to(torch.bfloat16)
+    gv, gl, ga = msda.backward(t["value"], t["spatial_shapes"], t["level_start_index"], t["sampling_locations"],
+                               t["attention_weights"], t["grad_out"], accum="fp32", grad_value=start.clone(),
+                               accumulate=True, workspace=ws, workspace_zeroed=zeroed)
+    torch.cuda.synchronize()
+    if zeroed:
+        assert int(torch.count_nonzero(ws)) == 0
+    rgv, rgl, rga = oracle.backward(inp, "bf16")
+    assert_grad("bf16", f64(gv), rgv + f64(start), "grad_value")
+    assert_grad("bf16", f64(gl), rgl, "grad_loc")
+    assert_grad("bf16", f64(ga), rga, "grad_attn")
+
+
 @pytest.mark.parametrize("levels_reversed,zeroed,big0", [(False, False, False), (True, False, False),
                                                           (False, True, False), (False, False, True),
                                                           (True, True, True)])
