@@ -93,3 +93,28 @@ def test_oracle_sample_is_batch0_prefix(bench):
     assert sub["value"].shape[0] == 1 and sub["sampling_locations"].shape[:2] == (1, 4)
     assert np.array_equal(sub["grad_out"], inp["grad_out"][:1, :4])
     assert bench.oracle_sample(wl, inp, 1e9)[1] == wl.Qn
+
+
+def test_fp32_backward_roofline_group(bench):
+    """With the FP32 accumulator the roofline takes the backward whole: the
+    backward kernel's, the rounding's and the touch count's bytes over the wall
+    time of the backward call (its kernels overlap on two streams), not the sum
+    of the traced kernel times; the compulsory fraction uses that wall time too."""
+    wl = W.WORKLOADS["stress_bf16"]
+    model = bench.byte_model(wl, corners=80_000_000, unique_rows=28_000_000)
+    kernels = {"forward": {"launches": 4, "avg_ms": 0.8, "ms_per_step": 0.8, "steps": 4},
+               "touch_count": {"launches": 4, "avg_ms": 0.2, "ms_per_step": 0.2, "steps": 4},
+               "backward": {"launches": 16, "avg_ms": 1.0, "ms_per_step": 4.0, "steps": 4},
+               "convert": {"launches": 8, "avg_ms": 1.0, "ms_per_step": 2.0, "steps": 4}}
+    per = {k: [v["avg_ms"]] * v["launches"] for k, v in kernels.items()}
+    r = bench.roofline_of("backward", per, wl, model, "fp32", 126 << 20, kernels, bwd_wall_ms=4.1)
+    alg = model["backward"] + model["convert"] + model["touch_count"]
+    assert r["kernel"] == "backward+convert" and r["algorithmic_bytes"] == alg
+    assert r["ms_per_step"] == 4.1 and r["launches_per_step"] == 7.0
+    assert math.isclose(r["achieved"], alg / 4.1e-3 / 1e9, rel_tol=1e-4)
+    assert "wall time" in r["time_source"]
+    # without the wall time: the traced kernels' sum
+    r2 = bench.roofline_of("backward", per, wl, model, "fp32", 126 << 20, kernels)
+    assert r2["ms_per_step"] == 6.2 and "time_source" not in r2
+    uf = bench.unique_fractions(model, kernels, 6781.1, 4.1)
+    assert math.isclose(uf["backward_frac"], model["bwd_total_unique"] / 4.1e-3 / 1e9 / 6781.1, rel_tol=1e-3)
