@@ -2204,9 +2204,12 @@ __global__ void __launch_bounds__(kBlockThreads) msda_convert_kernel(float* ws, 
 // MSDA_BWD_WORKSPACE_ZEROED).  Measured on GB300 (stress rounding, 8.6 GB of
 // workspace): 1.36 ms, against 1.41 ms for one thread per group of eight
 // elements (two groups in flight, eight blocks an SM; four groups 1.53 ms,
-// eight 1.92 ms; with a test of the values before re-zeroing 1.49 ms).
+// eight 1.92 ms; with a test of the values before re-zeroing 1.49 ms).  Held
+// to six blocks an SM (one 16-byte slot a lane: wider rows would spill), with
+// the classes worked out an iteration ahead: 1.32 ms alone, and the stress
+// backward with the rounding beside the coarse passes 4.23 -> 4.13 ms.
 template <typename T, int NV>
-__global__ void __launch_bounds__(kBlockThreads) msda_round_rows_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(kBlockThreads, NV == 1 ? 6 : 1) msda_round_rows_kernel(const KernelArgs a) {
     static_assert(sizeof(T) == 2, "16-bit grad_value");
     const T* tag = nullptr;
     __shared__ long long lo_hi[2];
@@ -2226,11 +2229,13 @@ __global__ void __launch_bounds__(kBlockThreads) msda_round_rows_kernel(const Ke
         const float* ws = reinterpret_cast<const float*>(a.grad_acc) + img * a.slice;
         float* wz = reinterpret_cast<float*>(a.grad_acc) + img * a.slice;
         T* gv = reinterpret_cast<T*>(a.conv_out) + img * a.slice;
-        for (long long base = r_lo + warp * 32; base < r_hi; base += nwarps * 32) {
-            // class of row base + lane: 0 untouched (sparse level), 1 written by its
-            // pass, 2 in the workspace (every row of a dense level); 1 past the range
-            const long long r = base + lane;
-            unsigned cls = r < r_hi ? 2u : 1u;
+        // class of row bb + lane: 0 untouched (sparse level), 1 written by its
+        // pass, 2 in the workspace (every row of a dense level); 1 past the range.
+        // Worked out one iteration ahead, so that its touch word's load overlaps
+        // the rows of the iteration before.
+        auto class_of = [&](long long bb) -> unsigned {
+            const long long r = bb + lane;
+            unsigned c = r < r_hi ? 2u : 1u;
             if (a.touch && r < r_hi) {
                 const unsigned row = (unsigned)r;
                 bool sp = false;
@@ -2238,9 +2243,15 @@ __global__ void __launch_bounds__(kBlockThreads) msda_round_rows_kernel(const Ke
                 if (sp) {
                     const unsigned pix = fdiv(row, a.div_m);
                     const unsigned id = ((unsigned)img * (unsigned)a.M + (row - pix * (unsigned)a.M)) * (unsigned)a.S + pix;
-                    cls = min(touch_bits(__ldg(a.touch + (id >> 4)), id), 2u);
+                    c = min(touch_bits(__ldg(a.touch + (id >> 4)), id), 2u);
                 }
             }
+            return c;
+        };
+        unsigned cls_next = class_of(r_lo + warp * 32);
+        for (long long base = r_lo + warp * 32; base < r_hi; base += nwarps * 32) {
+            const unsigned cls = cls_next;
+            cls_next = class_of(base + nwarps * 32);
 #pragma unroll
             for (int q0 = 0; q0 < 8; q0 += 4) {
                 unsigned c4[4];
