@@ -196,7 +196,7 @@ int ilog2_floor(int v) {
 // MSDA_TUNE is a comma-separated list of: C=<lanes>, P=<lanes>,
 // params=bulk|ld|direct, generic, spec, notma, tma, pointparallel, nopdl,
 // merge, nomerge, tiled, notiled, tp=<rows>, levelpass, nolevelpass, touch, notouch, tau=<n>, fold, nofold,
-// overlap, nooverlap, nol2hint, c8, noc8, nobwdhint, bwdhint=<n>.
+// overlap, nooverlap, nol2hint, c8, noc8.
 // None of them changes results beyond the rounding order of the grad_value sums.
 
 struct Tune {
@@ -217,7 +217,6 @@ struct Tune {
     int overlap = -1;      // touch classes: rounding of the finished rows on a second stream: -1 default, 0 off (nooverlap), 1 on (overlap)
     bool l2hint = true;    // TMA-gather forward: evict-first for levels over twice the L2 (off: nol2hint)
     int c8 = -1;           // backward into the FP32 workspace, eight lanes a unit: -1 default, 0 off (noc8), 1 on (c8)
-    int bwdhint = 1;       // eight-lane passes: evict-first for a level over twice the L2 (1), over half (2), any (3), off (0)
 };
 const Tune& tune() {
     static Tune t = [] {
@@ -255,8 +254,6 @@ const Tune& tune() {
             else if (!strcmp(tok, "nol2hint")) r.l2hint = false;
             else if (!strcmp(tok, "c8")) r.c8 = 1;
             else if (!strcmp(tok, "noc8")) r.c8 = 0;
-            else if (!strcmp(tok, "nobwdhint")) r.bwdhint = 0;
-            else if (!strncmp(tok, "bwdhint=", 8)) r.bwdhint = atoi(tok + 8);
         }
         return r;
     }();
@@ -1247,10 +1244,6 @@ msda_status backward_core(msda_dtype dt, msda_accum mode, unsigned flags, const 
         a.tpb = msda::kBlockThreads / 8;
         pl.smem = 0;
         pl.grid = dim3((unsigned)((d.units + a.tpb - 1) / a.tpb));
-        // the pass of a level whose rows take at least twice the L2 loads them,
-        // and stores its class-1 rows, evict-first (the threshold is 2 * l2_bytes)
-        const int bh = tune().bwdhint;
-        a.l2_bytes = bh == 1 ? di->l2_bytes : bh == 2 ? di->l2_bytes / 4 : bh >= 3 ? 1 : 0;
     }
     // With the rounding folded into the passes from level 2 on, the rows below
     // level 2's first row, final once passes 0 and 1 are done, are rounded by

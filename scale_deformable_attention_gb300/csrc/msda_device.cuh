@@ -1626,28 +1626,6 @@ __device__ __forceinline__ void unpack8(const uint2& w, float (&f)[4], const __h
     f[3] = b.y;
 }
 
-// Four 16-bit channels loaded, and stored, with an evict-first L2 policy: the
-// rows of a level over twice the L2 are read about once each in its pass, so
-// that the workspace rows their sums go to keep the L2.
-__device__ __forceinline__ uint2 ldg_evict_first(const uint2* p) {
-    uint2 r;
-    asm("{\n\t.reg .b64 pol;\n\t"
-        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
-        "ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], pol;\n\t}"
-        : "=r"(r.x), "=r"(r.y)
-        : "l"(p));
-    return r;
-}
-template <typename T>
-__device__ __forceinline__ void store4_evict_first(T* p, float a, float b, float c, float d) {
-    const T* tag = nullptr;
-    asm volatile("{\n\t.reg .b64 pol;\n\t"
-                 "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
-                 "st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, pol;\n\t}" ::"l"(p),
-                 "r"(pack2(a, b, tag)), "r"(pack2(c, d, tag))
-                 : "memory");
-}
-
 constexpr int kC8 = 8;
 
 template <typename T, int NV, bool TOUCH>
@@ -1688,13 +1666,6 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd8_kernel(const KernelAr
     }
     T* gl = reinterpret_cast<T*>(a.grad_loc);
     T* ga = reinterpret_cast<T*>(a.grad_attn);
-    // a pass over one level whose rows (one image's) take at least twice
-    // l2_bytes: its corner rows and its class-1 stores evict first (l2_bytes 0: off)
-    bool ef = false;
-    if (a.l2_bytes > 0 && a.s_end - a.s_begin <= a.K) {
-        const Level& v = lv[fdiv((uint32_t)a.s_begin, a.div_k)];
-        ef = v.ok && (long long)v.fH * v.W * a.M * a.D * (long long)sizeof(T) >= 2 * a.l2_bytes;
-    }
 
     for (int r0 = a.s_begin; r0 < a.s_end; r0 += kC8) {
         const int nj = min(kC8, a.s_end - r0);   // samples of this round (the same for the whole warp)
@@ -1738,11 +1709,10 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd8_kernel(const KernelAr
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
 #pragma unroll
-                    for (int n = 0; n < NV; ++n) {
-                        const uint2* q = reinterpret_cast<const uint2*>(vbase + off[k] + 32 * n);
-                        raw[jj][k][n] = ((st[jj].mask >> k) & 1u) ? (ef ? ldg_evict_first(q) : __ldg(q))
-                                                                   : make_uint2(0u, 0u);
-                    }
+                    for (int n = 0; n < NV; ++n)
+                        raw[jj][k][n] = ((st[jj].mask >> k) & 1u)
+                                            ? __ldg(reinterpret_cast<const uint2*>(vbase + off[k] + 32 * n))
+                                            : make_uint2(0u, 0u);
             }
 #pragma unroll
             for (int jj = 0; jj < JB; ++jj) {
@@ -1832,10 +1802,9 @@ __global__ void __launch_bounds__(kBlockThreads) msda_bwd8_kernel(const KernelAr
                 for (int n = 0; n < NV; ++n) {
                     const float2 t0 = __fmul2_rn(cf, make_float2(g[n][0], g[n][1]));
                     const float2 t1 = __fmul2_rn(cf, make_float2(g[n][2], g[n][3]));
-                    if (TOUCH && ((scls >> (2 * k)) & 3u) == 1u) {   // the row's one contribution
-                        if (ef) store4_evict_first<T>(tbase + off[k] + 32 * n, t0.x, t0.y, t1.x, t1.y);
-                        else store4<T>(tbase + off[k] + 32 * n, t0.x, t0.y, t1.x, t1.y);
-                    } else
+                    if (TOUCH && ((scls >> (2 * k)) & 3u) == 1u)
+                        store4<T>(tbase + off[k] + 32 * n, t0.x, t0.y, t1.x, t1.y);   // the row's one contribution
+                    else
                         red_v4_f32(gbase + off[k] + 32 * n, t0.x, t0.y, t1.x, t1.y);
                 }
             }

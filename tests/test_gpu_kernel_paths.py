@@ -7,8 +7,7 @@ the FP32 accumulator on chip forced on (with tiles of 16 rows: most points
 straddle tiles) and off, and the backward run one pass per level (with and
 without the corner merge, with the touch classes of the FP32 workspace's
 rows off, with every level or no level sparse, with four lanes a unit
-instead of eight, with the evict-first loads and stores of the eight-lane
-passes on every level) or in one pass.  Each runs in a
+instead of eight) or in one pass.  Each runs in a
 child process with MSDA_TUNE set."""
 import os
 import subprocess
@@ -24,7 +23,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
                                   "merge", "nomerge", "nopdl", "merge,P=2", "spec", "tiled", "tiled,tp=16", "notiled",
                                   "levelpass", "levelpass,merge", "nolevelpass", "levelpass,nomerge",
                                   "levelpass,notouch", "levelpass,tau=1", "levelpass,tau=1000", "levelpass,overlap",
-                                  "levelpass,noc8", "levelpass,c8,notouch", "levelpass,bwdhint=3"])
+                                  "levelpass,noc8", "levelpass,c8,notouch"])
 def test_kernel_family(tune):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
