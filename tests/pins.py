@@ -244,6 +244,85 @@ def pin_zero_padding():
     _close(gv[0, :, 0].reshape(4, 5, D), ev, 1e-15, what="edge grad_value")
 
 
+def pin_thin_levels():
+    """Levels one pixel high or wide (msda-triton README "The operator": the
+    corners of x*W - 0.5 with zero padding).  On a 1x1 level bilinear
+    sampling with zero padding is the tent (1 - |x_im|)(1 - |y_im|) times the
+    pixel, so grad_attn = tent * <g, v>, grad_value = A * tent * g and the
+    location gradient is A * <g, v> times -sign(x_im) * W (y: -sign(y_im) * H)
+    times the other axis' tent.  On a level one pixel high the x axis is
+    piecewise-linear interpolation of the row padded with zeros (np.interp)
+    times the y tent.  Samples keep clear of the kinks (x_im, y_im in
+    {-1, 0, 1} and the integers of the row)."""
+    rng = np.random.default_rng(21)
+    Q, D = 40, 3
+    g = rng.standard_normal((1, Q, D))
+    a = rng.uniform(-1, 1, (1, Q, 1, 1, 1))
+
+    def away(n):   # locations in [-0.3, 1.3] at least 0.02 from the kinks of a level n pixels across
+        u = rng.uniform(-0.3, 1.3, 4 * Q)
+        t = u * n - 0.5
+        keep = np.abs(t - np.round(t)) > 0.02
+        return u[keep][:Q]
+
+    # 1x1: the tent on both axes
+    v = rng.standard_normal((1, 1, 1, D))
+    loc = np.stack([away(1), away(1)], -1).reshape(1, Q, 1, 1, 1, 2)
+    inp = _inputs(v, ((1, 1),), loc, a, g)
+    xi, yi = loc[0, :, 0, 0, 0, 0] - 0.5, loc[0, :, 0, 0, 0, 1] - 0.5
+    tx, ty = np.maximum(0.0, 1 - np.abs(xi)), np.maximum(0.0, 1 - np.abs(yi))
+    A = a.reshape(Q)
+    out = oracle.forward(inp, "f64", coord_mode=0).reshape(Q, D)
+    _close(out, (A * tx * ty)[:, None] * v.reshape(1, D), 1e-14, what="1x1 level out")
+    gv, gl, ga = oracle.backward(inp, "f64", coord_mode=0)
+    gvv = g.reshape(Q, D) @ v.reshape(D)
+    _close(ga.reshape(Q), tx * ty * gvv, 1e-14, what="1x1 level grad_attn")
+    _close(gv.reshape(D), ((A * tx * ty)[:, None] * g.reshape(Q, D)).sum(0), 1e-14, what="1x1 level grad_value")
+    sx = np.where(np.abs(xi) < 1, -np.sign(xi), 0.0)
+    sy = np.where(np.abs(yi) < 1, -np.sign(yi), 0.0)
+    _close(gl.reshape(Q, 2), np.stack([A * gvv * sx * ty, A * gvv * sy * tx], -1), 1e-14,
+           what="1x1 level grad_loc")
+
+    # one pixel high, five wide: np.interp along x, the tent along y
+    Wd = 5
+    v = rng.standard_normal((1, Wd, 1, D))
+    loc = np.stack([away(Wd), away(1)], -1).reshape(1, Q, 1, 1, 1, 2)
+    inp = _inputs(v, ((1, Wd),), loc, a)
+    xi, yi = loc[0, :, 0, 0, 0, 0] * Wd - 0.5, loc[0, :, 0, 0, 0, 1] - 0.5
+    ty = np.maximum(0.0, 1 - np.abs(yi))
+    xs = np.arange(-1, Wd + 1)
+    row = np.zeros((Wd + 2, D))
+    row[1:-1] = v.reshape(Wd, D)
+    exp = np.stack([np.interp(xi, xs, row[:, d]) for d in range(D)], -1) * (A * ty)[:, None]
+    out = oracle.forward(inp, "f64", coord_mode=0).reshape(Q, D)
+    _close(out, exp, 1e-14, what="one-pixel-high level out")
+
+    # one pixel wide, four high: the same with the axes exchanged; the location
+    # gradient from the interpolant's slope (a central difference of np.interp
+    # inside one linear piece is exact) and the x tent's
+    Hd = 4
+    v = rng.standard_normal((1, Hd, 1, D))
+    loc = np.stack([away(1), away(Hd)], -1).reshape(1, Q, 1, 1, 1, 2)
+    inp = _inputs(v, ((Hd, 1),), loc, a, g)
+    xi, yi = loc[0, :, 0, 0, 0, 0] - 0.5, loc[0, :, 0, 0, 0, 1] * Hd - 0.5
+    tx = np.maximum(0.0, 1 - np.abs(xi))
+    ys = np.arange(-1, Hd + 1)
+    col = np.zeros((Hd + 2, D))
+    col[1:-1] = v.reshape(Hd, D)
+    iy = np.stack([np.interp(yi, ys, col[:, d]) for d in range(D)], -1)
+    exp = iy * (A * tx)[:, None]
+    out = oracle.forward(inp, "f64", coord_mode=0).reshape(Q, D)
+    _close(out, exp, 1e-14, what="one-pixel-wide level out")
+    h = 0.01
+    slope = np.stack([(np.interp(yi + h, ys, col[:, d]) - np.interp(yi - h, ys, col[:, d])) / (2 * h)
+                      for d in range(D)], -1)
+    gq = g.reshape(Q, D)
+    sx = np.where(np.abs(xi) < 1, -np.sign(xi), 0.0)
+    egl = np.stack([A * 1 * sx * (gq * iy).sum(-1), A * Hd * tx * (gq * slope).sum(-1)], -1)
+    gv, gl, ga = oracle.backward(inp, "f64", coord_mode=0)
+    _close(gl.reshape(Q, 2), egl, 1e-12, what="one-pixel-wide level grad_loc")
+
+
 def pin_convexity():
     """sum A = 1, A >= 0, corners inside: each output channel lies within the
     range of the corner values the unit read."""
@@ -588,7 +667,7 @@ def pin_fused_fp32_location():
 
 ALL_PINS = [
     pin_hand_worked, pin_constant_field, pin_linear_field, pin_pixel_centres, pin_zero_padding,
-    pin_convexity, pin_gridsample, pin_brute_force, pin_finite_differences, pin_adjoint,
+    pin_thin_levels, pin_convexity, pin_gridsample, pin_brute_force, pin_finite_differences, pin_adjoint,
     pin_scatter_total, pin_fp32_coordinate, pin_coordinate_modes_agree, pin_samplers,
     pin_fused_special_cases, pin_fused_torch_restatement, pin_fused_finite_differences,
     pin_fused_coordinate_modes_agree, pin_fused_fp32_location,
